@@ -1,0 +1,223 @@
+"""CPU oracle for the normalize-then-quantize path: TEST INFRASTRUCTURE ONLY.
+
+Python view of ``fp8norm_oracle.c`` (loaded through ctypes).  Only the tests,
+``__graft_entry__.smoke()`` and the benchmark's CPU-baseline leg may import this
+package; the product library (``rmsnorm_fp8_activation_gb300``) never does.
+
+Arrays: bf16 tensors are ``numpy.uint16`` bit patterns, e4m3 and E8M0 tensors
+are ``numpy.uint8`` codes, scales and descales are ``numpy.float32``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+from . import build as _build
+
+ACT_SIGMOID = 0
+ACT_SILU = 1
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """Load (building first if needed) the oracle shared library."""
+    global _lib
+    if _lib is None:
+        _lib = load_library(_build.build())
+    return _lib
+
+
+def use_library(L) -> None:
+    """Route every function of this module through the library ``L`` (a
+    ``load_library`` result).  The mutation tests use it to run the pins
+    against a copy of the oracle with a planted mistake."""
+    global _lib
+    _lib = L
+
+
+def load_library(path: str) -> ctypes.CDLL:
+    """Open an oracle shared library and declare its signatures."""
+    L = ctypes.CDLL(path)
+    P = ctypes.c_void_p
+    i64, i32, f32 = ctypes.c_int64, ctypes.c_int32, ctypes.c_float
+    L.oracle_bf16_to_double.argtypes = [ctypes.c_uint16]
+    L.oracle_bf16_to_double.restype = ctypes.c_double
+    L.oracle_bf16_from_double.argtypes = [ctypes.c_double]
+    L.oracle_bf16_from_double.restype = ctypes.c_uint16
+    L.oracle_e4m3_to_double.argtypes = [ctypes.c_uint8]
+    L.oracle_e4m3_to_double.restype = ctypes.c_double
+    L.oracle_e4m3_from_float.argtypes = [f32]
+    L.oracle_e4m3_from_float.restype = ctypes.c_uint8
+    L.oracle_act_bf16.argtypes = [ctypes.c_uint16, ctypes.c_int]
+    L.oracle_act_bf16.restype = ctypes.c_uint16
+    L.oracle_bf16_from_float_n.argtypes = [P, i64, P]
+    L.oracle_bf16_from_float_n.restype = None
+    L.oracle_e4m3_from_float_n.argtypes = [P, i64, P]
+    L.oracle_e4m3_from_float_n.restype = None
+    L.oracle_act_bf16_n.argtypes = [P, i64, ctypes.c_int, P]
+    L.oracle_act_bf16_n.restype = None
+    L.oracle_mean_square_bf16.argtypes = [P, i64]
+    L.oracle_mean_square_bf16.restype = f32
+    L.oracle_rms_factor.argtypes = [f32, f32]
+    L.oracle_rms_factor.restype = f32
+    L.oracle_e8m0_code.argtypes = [ctypes.c_uint16]
+    L.oracle_e8m0_code.restype = ctypes.c_uint8
+    L.oracle_gated_rmsnorm_quant_token.argtypes = [
+        P, i64, P, i64, P, i64, i32, i32, f32, ctypes.c_int, P, i64, P]
+    L.oracle_gated_rmsnorm_quant_token.restype = None
+    L.oracle_gated_rmsnorm_quant_one.argtypes = [
+        P, P, P, i32, i32, f32, ctypes.c_int, P, P, P]
+    L.oracle_gated_rmsnorm_quant_one.restype = None
+    L.oracle_rmsnorm_quant_mx.argtypes = [
+        P, i64, P, i32, P, i64, P, i32, i64, f32, P, i64, P, i64, P, i64]
+    L.oracle_rmsnorm_quant_mx.restype = None
+    L.oracle_static_head_quant.argtypes = [P, i64, i64, i64, i32, i32, P, P]
+    L.oracle_static_head_quant.restype = None
+    return L
+
+
+def _ptr(a: np.ndarray) -> int:
+    return a.ctypes.data
+
+
+def _c(a, dtype) -> np.ndarray:
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+# ---- codecs ---------------------------------------------------------------
+
+def bf16_to_float(bits) -> np.ndarray:
+    """Exact float32 values of bf16 bit patterns (vectorised bit shift)."""
+    b = np.asarray(bits, dtype=np.uint16)
+    return (b.astype(np.uint32) << 16).view(np.float32)
+
+
+def bf16_from_double(v: float) -> int:
+    return int(lib().oracle_bf16_from_double(float(v)))
+
+
+def e4m3_to_double(code: int) -> float:
+    return float(lib().oracle_e4m3_to_double(int(code)))
+
+
+def e4m3_from_float(v: float) -> int:
+    return int(lib().oracle_e4m3_from_float(float(v)))
+
+
+def act_bf16(g: int, act: int) -> int:
+    return int(lib().oracle_act_bf16(int(g), int(act)))
+
+
+def bf16_from_float_n(v) -> np.ndarray:
+    """bf16 bits of binary32 values, nearest-even."""
+    v = _c(v, np.float32)
+    out = np.empty(v.shape, dtype=np.uint16)
+    lib().oracle_bf16_from_float_n(_ptr(v), v.size, _ptr(out))
+    return out
+
+
+def e4m3_from_float_n(v) -> np.ndarray:
+    """Saturating nearest-even E4M3 codes of binary32 values."""
+    v = _c(v, np.float32)
+    out = np.empty(v.shape, dtype=np.uint8)
+    lib().oracle_e4m3_from_float_n(_ptr(v), v.size, _ptr(out))
+    return out
+
+
+def act_bf16_n(g, act: int) -> np.ndarray:
+    g = _c(g, np.uint16)
+    out = np.empty(g.shape, dtype=np.uint16)
+    lib().oracle_act_bf16_n(_ptr(g), g.size, int(act), _ptr(out))
+    return out
+
+
+def act_table(act: int) -> np.ndarray:
+    """bf16(act(g)) for all 65536 gate bit patterns."""
+    return act_bf16_n(np.arange(65536, dtype=np.uint16), act)
+
+
+def mean_square(x_bits) -> float:
+    x = _c(x_bits, np.uint16)
+    return float(lib().oracle_mean_square_bf16(_ptr(x), x.size))
+
+
+def rms_factor(ms: float, eps: float) -> float:
+    return float(lib().oracle_rms_factor(ms, eps))
+
+
+def e8m0_code(amax_bits: int) -> int:
+    return int(lib().oracle_e8m0_code(int(amax_bits)))
+
+
+# ---- operations -----------------------------------------------------------
+
+def gated_rmsnorm_quant_token(x, gate, weight, eps: float, act: int):
+    """Operation (A).  x, gate: uint16 [T, H, D]; weight: uint16 [D].
+
+    Returns (codes uint8 [T, H*D], scale float32 [T]).
+    """
+    x = _c(x, np.uint16)
+    gate = _c(gate, np.uint16)
+    weight = _c(weight, np.uint16)
+    T, H, D = x.shape
+    out = np.zeros((T, H * D), dtype=np.uint8)
+    scale = np.zeros((T,), dtype=np.float32)
+    lib().oracle_gated_rmsnorm_quant_token(
+        _ptr(x), H * D, _ptr(gate), H * D, _ptr(weight), T, H, D, float(eps), int(act),
+        _ptr(out), H * D, _ptr(scale))
+    return out, scale
+
+
+def gated_rmsnorm_quant_one(x_tok, gate_tok, weight, eps: float, act: int):
+    """Operation (A) on one token.  x_tok, gate_tok: uint16 [H, D].
+
+    Returns (y bf16 bits [H*D], codes uint8 [H*D], scale float).
+    """
+    x_tok = _c(x_tok, np.uint16)
+    gate_tok = _c(gate_tok, np.uint16)
+    weight = _c(weight, np.uint16)
+    H, D = x_tok.shape
+    y = np.zeros((H * D,), dtype=np.uint16)
+    out = np.zeros((H * D,), dtype=np.uint8)
+    scale = np.zeros((1,), dtype=np.float32)
+    lib().oracle_gated_rmsnorm_quant_one(
+        _ptr(x_tok), _ptr(gate_tok), _ptr(weight), H, D, float(eps), int(act),
+        _ptr(y), _ptr(out), _ptr(scale))
+    return y, out, float(scale[0])
+
+
+def rmsnorm_quant_mx(q, q_weight, kv, kv_weight, eps: float):
+    """Operation (B).  q: uint16 [M, Nq]; kv: uint16 [M, Nkv].
+
+    Returns (q codes uint8 [M, Nq], q scales uint8 [M, Nq/32], kv bf16 bits [M, Nkv]).
+    """
+    q = _c(q, np.uint16)
+    kv = _c(kv, np.uint16)
+    q_weight = _c(q_weight, np.uint16)
+    kv_weight = _c(kv_weight, np.uint16)
+    M, Nq = q.shape
+    M2, Nkv = kv.shape
+    assert M == M2 and Nq % 32 == 0
+    q_out = np.zeros((M, Nq), dtype=np.uint8)
+    q_scale = np.zeros((M, Nq // 32), dtype=np.uint8)
+    kv_out = np.zeros((M, Nkv), dtype=np.uint16)
+    lib().oracle_rmsnorm_quant_mx(
+        _ptr(q), Nq, _ptr(q_weight), Nq, _ptr(kv), Nkv, _ptr(kv_weight), Nkv, M, float(eps),
+        _ptr(q_out), Nq, _ptr(q_scale), Nq // 32, _ptr(kv_out), Nkv)
+    return q_out, q_scale, kv_out
+
+
+def static_head_quant(x, descale):
+    """Operation (C) on one tensor.  x: uint16 [T, H, Dh]; descale: float32 [H].
+
+    Returns codes uint8 [T, H, Dh].
+    """
+    x = _c(x, np.uint16)
+    descale = _c(descale, np.float32)
+    T, H, Dh = x.shape
+    out = np.zeros((T, H, Dh), dtype=np.uint8)
+    lib().oracle_static_head_quant(_ptr(x), H * Dh, Dh, T, H, Dh, _ptr(descale), _ptr(out))
+    return out
