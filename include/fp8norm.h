@@ -1,0 +1,188 @@
+/*
+ * libfp8norm: row-wise normalize-then-quantize for GB300 (sm_103a).
+ *
+ * C ABI.  Every operation takes caller-owned DEVICE pointers, plain sizes and
+ * strides (in elements), and the caller's cudaStream_t; it validates its
+ * arguments on the host, enqueues exactly one kernel on that stream and
+ * returns without synchronising, so the calls can be captured in a CUDA graph.
+ * The operations allocate no memory and keep no state between calls.
+ *
+ * Element encodings: bf16 inputs/outputs are bfloat16 bit patterns (uint16);
+ * e4m3 outputs are OCP FP8 E4M3 ("fn": bias 7, max 448, NaN 0x7F/0xFF, no
+ * infinities); E8M0 scales are OCP MX exponent codes (value 2^(code - 127),
+ * 0xFF = NaN).  "RN32" is IEEE binary32 round-to-nearest-even, "bf16()"
+ * round-to-nearest-even to bfloat16, "e4m3()" saturating round-to-nearest-even
+ * to E4M3 (|v| >= 448 -> +-448, sign of zero kept).
+ *
+ * Alignment: every tensor pointer must be 16-byte aligned, and every row
+ * stride must keep rows 16-byte aligned (a multiple of 8 bf16 elements, of 16
+ * e4m3 / E8M0 bytes for the MX q output and scale rows; see each call).
+ *
+ * Errors: a nonzero fp8n_status is returned and nothing is enqueued when an
+ * argument is invalid.  FP8N_ERR_CUDA means a CUDA call failed; the CUDA error
+ * code is then available from fp8n_last_cuda_error() on the calling thread.
+ * A zero-sized problem (T == 0, M == 0) returns FP8N_OK without a launch.
+ *
+ * Optional device status word (uint32_t*, may be NULL): kernels OR bits into
+ * it and never clear it: FP8N_STATUS_BAD_DESCALE (a descale that is not finite
+ * and positive was used), FP8N_STATUS_PIPELINE_TIMEOUT (a pipeline wait gave
+ * up after its iteration limit; the outputs of that launch are incomplete).
+ */
+#ifndef FP8NORM_H
+#define FP8NORM_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* fp8n_stream_t; /* the same type as cudaStream_t */
+
+typedef enum {
+  FP8N_OK = 0,
+  FP8N_ERR_NULL = 1,        /* a required pointer is NULL */
+  FP8N_ERR_SHAPE = 2,       /* negative or inconsistent sizes / strides */
+  FP8N_ERR_MISALIGNED = 3,  /* a pointer or stride breaks the 16-byte rule */
+  FP8N_ERR_UNSUPPORTED = 4, /* a size outside the supported range */
+  FP8N_ERR_BAD_SCALE = 5,   /* fp8n_check_descales found a bad descale */
+  FP8N_ERR_CUDA = 6         /* a CUDA runtime call failed */
+} fp8n_status;
+
+typedef enum { FP8N_ACT_SIGMOID = 0, FP8N_ACT_SILU = 1 } fp8n_act;
+
+#define FP8N_STATUS_BAD_DESCALE 0x1u
+#define FP8N_STATUS_PIPELINE_TIMEOUT 0x2u
+
+/* Human-readable name of a status code (static storage). */
+const char* fp8n_status_string(fp8n_status s);
+
+/* cudaError_t of the last FP8N_ERR_CUDA returned on this thread (0 if none). */
+int fp8n_last_cuda_error(void);
+
+/* Library version as 0xMMmmpp. */
+uint32_t fp8n_version(void);
+
+/*
+ * (A) Gated RMSNorm fused with per-token dynamic FP8 quantisation.
+ *
+ * Source: "[ROCm][Kimi-K3] Fuse gated RMSNorm with per-token FP8 for KDA
+ * o_proj" (vLLM PR 54254): Purpose (one kernel for gated RMSNorm and per-token
+ * amax FP8 ahead of the o_proj GEMM); Tests (checked against sequential gated
+ * RMSNorm + per-token amax); review thread on the torch reference helper and
+ * the wrapper.
+ *
+ * For each token t and head h (per-head RMS over D):
+ *   ms  = RN32(sum_d x[t,h,d]^2 / D)          (sum exact, order independent)
+ *   r   = RN32(1 / RN32(sqrt(RN32(ms + eps))))
+ *   y   = bf16( bf16(bf16(RN32(x * r)) * w[d]) * bf16(act(gate[t,h,d])) )
+ * act is sigmoid or silu(g) = g * sigmoid(g), correctly rounded to bf16.
+ * Per token (one scale over all H*D values):
+ *   scale[t] = RN32(max|y| / 448);  out[t, h*D + d] = e4m3(RN32(y / scale[t]))
+ * A token with max|y| == 0 gets scale 0 and zero codes carrying the sign of y.
+ *
+ * x, gate : bf16 [T, H, D]; heads contiguous inside a token; token strides
+ *           x_stride / gate_stride (elements, multiples of 8, >= H*D).
+ * weight  : bf16 [D], shared by all heads.
+ * out     : e4m3 [T, H*D], token stride out_stride (bytes = elements,
+ *           multiple of 16, >= H*D).
+ * scale   : fp32 [T].
+ * Limits  : D a multiple of 8, 8 <= D <= 8192, H >= 1, H*D <= 16384,
+ *           eps finite and >= 0; otherwise FP8N_ERR_UNSUPPORTED / _SHAPE.
+ */
+fp8n_status fp8n_gated_rmsnorm_quant_token(const void* x, int64_t x_stride, const void* gate,
+                                           int64_t gate_stride, const void* weight, int64_t T,
+                                           int32_t H, int32_t D, float eps, fp8n_act act,
+                                           void* out, int64_t out_stride, float* scale,
+                                           uint32_t* status, fp8n_stream_t stream);
+
+/*
+ * (B) Fused q/kv RMSNorm: q leaves as MXFP8, kv as normalised bf16.
+ *
+ * Source: "[ROCm][Perf] FP8 o-projection for DeepSeek-V4.1-Flash MLA on AMD
+ * MI355X" (vLLM PR 57081), third commit message (one producer normalises q and
+ * kv, emits q as MXFP8 with row-major E8M0 scales, bitwise identical to the
+ * unfused steps); OCP Microscaling Formats v1.0 section 5 (block scale
+ * 2^(floor(log2 amax) - 8) for E4M3 elements).
+ *
+ * Per row m:  yq = bf16(bf16(RN32(q * r_q)) * q_weight), r_q over the whole q
+ * row as in (A); per 32-column block b of yq:
+ *   e = clamp(floor(log2 max|yq_b|) - 8, -127, 127)  (e = -127 if the block is 0)
+ *   q_scale[m, b] = e + 127;  q_out[m, 32b + j] = e4m3(yq * 2^-e)
+ * kv_out[m, :] = bf16(bf16(RN32(kv * r_kv)) * kv_weight).
+ *
+ * q     : bf16 [M, Nq], row stride q_stride (elements, multiple of 8).
+ * kv    : bf16 [M, Nkv], row stride kv_stride (elements, multiple of 8); may be
+ *         NULL when Nkv == 0.
+ * q_out : e4m3 [M, Nq], row stride q_out_stride (bytes, multiple of 16).
+ * q_scale: E8M0 uint8 [M, Nq/32] row-major, row stride q_scale_stride (bytes).
+ * kv_out: bf16 [M, Nkv], row stride kv_out_stride (elements, multiple of 8).
+ * Limits: Nq a multiple of 32 with 32 <= Nq <= 16384; Nkv a multiple of 8 with
+ *         0 <= Nkv <= 16384.
+ */
+fp8n_status fp8n_rmsnorm_quant_mx(const void* q, int64_t q_stride, const void* q_weight,
+                                  int32_t Nq, const void* kv, int64_t kv_stride,
+                                  const void* kv_weight, int32_t Nkv, int64_t M, float eps,
+                                  void* q_out, int64_t q_out_stride, uint8_t* q_scale,
+                                  int64_t q_scale_stride, void* kv_out, int64_t kv_out_stride,
+                                  uint32_t* status, fp8n_stream_t stream);
+
+/*
+ * (C) Static per-head FP8 quantisation of packed variable-length Q, K, V.
+ *
+ * Source: "[ROCm][MLA] Add guarded gfx942 FP8 context prefill" (vLLM PR
+ * 51551): Summary and "What this PR does" (static per-head Q/K/V scales from a
+ * calibrated artifact replace dynamic amax reductions; a one-kernel static
+ * quantizer; finite positive descales; 12 heads, D192 Q/K, D128 V).
+ *
+ *   q_out[t,h,d] = e4m3(RN32(q[t,h,d] / q_descale[h]))  and likewise for k, v,
+ * all three tensors in one launch.
+ *
+ * q, k     : bf16 [T, H, Dqk] with token stride qk_tok_stride and head stride
+ *            qk_head_stride (elements, multiples of 8); the d axis contiguous.
+ * v        : bf16 [T, H, Dv] with v_tok_stride, v_head_stride.
+ * descales : fp32 [H] each, device memory.  A descale that is not finite and
+ *            positive is still applied as an IEEE division and sets
+ *            FP8N_STATUS_BAD_DESCALE in *status (when status is not NULL).
+ * cu_seqlens: optional int32 [num_seqs + 1] device prefix sums of the packed
+ *            sequences (NULL allowed).  The map is elementwise, so it is only
+ *            carried for the caller's bookkeeping; T is the packed length.
+ * outputs  : e4m3, contiguous [T, H, Dqk] / [T, H, Dv].
+ * Limits   : Dqk, Dv multiples of 8 in [8, 8192]; H >= 1.
+ */
+fp8n_status fp8n_static_head_quant(const void* q, const void* k, const void* v,
+                                   int64_t qk_tok_stride, int64_t qk_head_stride,
+                                   int64_t v_tok_stride, int64_t v_head_stride, int64_t T,
+                                   int32_t H, int32_t Dqk, int32_t Dv, const float* q_descale,
+                                   const float* k_descale, const float* v_descale,
+                                   const int32_t* cu_seqlens, int32_t num_seqs, void* q_out,
+                                   void* k_out, void* v_out, uint32_t* status,
+                                   fp8n_stream_t stream);
+
+/*
+ * Gate activation alone: out[i] = bf16(act(g[i])), act = sigmoid or
+ * silu(g) = g * sigmoid(g), correctly rounded (nearest-even of the real
+ * function; limits at +-inf, NaN stays NaN).  This is the gate factor of (A),
+ * computed by the same device code; the source is the torch reference helper
+ * in "[ROCm][Kimi-K3] Fuse gated RMSNorm with per-token FP8 for KDA o_proj"
+ * (the gate enters through torch.sigmoid in the activation dtype).
+ * g, out: bf16 [n], 2-byte aligned device pointers; n >= 0.
+ */
+fp8n_status fp8n_gate_act_bf16(const void* g, int64_t n, fp8n_act act, void* out,
+                               fp8n_stream_t stream);
+
+/*
+ * Synchronous helper: reads n fp32 descales from device memory (through a
+ * host copy on `stream`, which it synchronises) and returns
+ * FP8N_ERR_BAD_SCALE unless every one is finite and > 0.  Source: the
+ * static-scale validation in "[ROCm][MLA] Add guarded gfx942 FP8 context
+ * prefill" (finite positive descales are checked before use; missing or
+ * incompatible scales fail instead of falling back).  Not for use inside a
+ * stream capture.  1 <= n <= 65536.
+ */
+fp8n_status fp8n_check_descales(const float* descale, int32_t n, fp8n_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

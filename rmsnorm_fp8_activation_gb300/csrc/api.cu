@@ -1,0 +1,197 @@
+// C ABI of libfp8norm: argument validation on the host, then one launch on the
+// caller's stream (see include/fp8norm.h for the contract of each call).
+#include <cmath>
+#include <cstdint>
+#include <vector>
+
+#include "fp8norm.h"
+#include "kernels.h"
+
+namespace {
+
+thread_local int g_last_cuda_error = 0;
+
+fp8n_status cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return FP8N_OK;
+  g_last_cuda_error = (int)e;
+  return FP8N_ERR_CUDA;
+}
+
+bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+}  // namespace
+
+namespace fp8n {
+
+int sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1) return 1;
+  return n;
+}
+
+}  // namespace fp8n
+
+extern "C" {
+
+const char* fp8n_status_string(fp8n_status s) {
+  switch (s) {
+    case FP8N_OK: return "FP8N_OK";
+    case FP8N_ERR_NULL: return "FP8N_ERR_NULL: a required pointer is NULL";
+    case FP8N_ERR_SHAPE: return "FP8N_ERR_SHAPE: negative or inconsistent sizes or strides";
+    case FP8N_ERR_MISALIGNED: return "FP8N_ERR_MISALIGNED: a pointer or stride breaks the 16-byte rule";
+    case FP8N_ERR_UNSUPPORTED: return "FP8N_ERR_UNSUPPORTED: a size outside the supported range";
+    case FP8N_ERR_BAD_SCALE: return "FP8N_ERR_BAD_SCALE: a descale is not finite and positive";
+    case FP8N_ERR_CUDA: return "FP8N_ERR_CUDA: a CUDA runtime call failed";
+  }
+  return "unknown fp8n_status";
+}
+
+int fp8n_last_cuda_error(void) { return g_last_cuda_error; }
+
+uint32_t fp8n_version(void) { return 0x000100u; }
+
+fp8n_status fp8n_gated_rmsnorm_quant_token(const void* x, int64_t x_stride, const void* gate,
+                                           int64_t gate_stride, const void* weight, int64_t T,
+                                           int32_t H, int32_t D, float eps, fp8n_act act,
+                                           void* out, int64_t out_stride, float* scale,
+                                           uint32_t* status, fp8n_stream_t stream) {
+  if (T < 0 || H < 1 || D < 1) return FP8N_ERR_SHAPE;
+  if (act != FP8N_ACT_SIGMOID && act != FP8N_ACT_SILU) return FP8N_ERR_UNSUPPORTED;
+  if (D % 8 != 0 || D > 8192 || (int64_t)H * D > 16384) return FP8N_ERR_UNSUPPORTED;
+  if (!(eps >= 0.0f) || std::isinf(eps)) return FP8N_ERR_UNSUPPORTED;
+  const int64_t row = (int64_t)H * D;
+  if (x_stride < row || gate_stride < row || out_stride < row) return FP8N_ERR_SHAPE;
+  if (T == 0) return FP8N_OK;
+  if (!x || !gate || !weight || !out || !scale) return FP8N_ERR_NULL;
+  if (!aligned16(x) || !aligned16(gate) || !aligned16(weight) || !aligned16(out) ||
+      x_stride % 8 || gate_stride % 8 || out_stride % 16 || ((uintptr_t)scale & 3u) ||
+      ((uintptr_t)status & 3u))
+    return FP8N_ERR_MISALIGNED;
+  fp8n::GatedParams p;
+  p.x = (const uint16_t*)x;
+  p.x_stride = x_stride;
+  p.gate = (const uint16_t*)gate;
+  p.gate_stride = gate_stride;
+  p.weight = (const uint16_t*)weight;
+  p.T = T;
+  p.H = H;
+  p.D = D;
+  p.eps = eps;
+  p.act = (int)act;
+  p.out = (uint8_t*)out;
+  p.out_stride = out_stride;
+  p.scale = scale;
+  p.status = status;
+  return cuda_status(fp8n::launch_gated(p, (cudaStream_t)stream));
+}
+
+fp8n_status fp8n_rmsnorm_quant_mx(const void* q, int64_t q_stride, const void* q_weight,
+                                  int32_t Nq, const void* kv, int64_t kv_stride,
+                                  const void* kv_weight, int32_t Nkv, int64_t M, float eps,
+                                  void* q_out, int64_t q_out_stride, uint8_t* q_scale,
+                                  int64_t q_scale_stride, void* kv_out, int64_t kv_out_stride,
+                                  uint32_t* status, fp8n_stream_t stream) {
+  if (M < 0 || Nq < 1 || Nkv < 0) return FP8N_ERR_SHAPE;
+  if (Nq % 32 != 0 || Nq > 16384 || Nkv % 8 != 0 || Nkv > 16384) return FP8N_ERR_UNSUPPORTED;
+  if (!(eps >= 0.0f) || std::isinf(eps)) return FP8N_ERR_UNSUPPORTED;
+  if (q_stride < Nq || q_out_stride < Nq || q_scale_stride < Nq / 32) return FP8N_ERR_SHAPE;
+  if (Nkv > 0 && (kv_stride < Nkv || kv_out_stride < Nkv)) return FP8N_ERR_SHAPE;
+  if (M == 0) return FP8N_OK;
+  if (!q || !q_weight || !q_out || !q_scale) return FP8N_ERR_NULL;
+  if (Nkv > 0 && (!kv || !kv_weight || !kv_out)) return FP8N_ERR_NULL;
+  if (!aligned16(q) || !aligned16(q_weight) || !aligned16(q_out) || q_stride % 8 ||
+      q_out_stride % 16 || ((uintptr_t)status & 3u))
+    return FP8N_ERR_MISALIGNED;
+  if (Nkv > 0 && (!aligned16(kv) || !aligned16(kv_weight) || !aligned16(kv_out) ||
+                  kv_stride % 8 || kv_out_stride % 8))
+    return FP8N_ERR_MISALIGNED;
+  fp8n::MxParams p;
+  p.q = (const uint16_t*)q;
+  p.q_stride = q_stride;
+  p.q_weight = (const uint16_t*)q_weight;
+  p.Nq = Nq;
+  p.kv = (const uint16_t*)kv;
+  p.kv_stride = kv_stride;
+  p.kv_weight = (const uint16_t*)kv_weight;
+  p.Nkv = Nkv;
+  p.M = M;
+  p.eps = eps;
+  p.q_out = (uint8_t*)q_out;
+  p.q_out_stride = q_out_stride;
+  p.q_scale = q_scale;
+  p.q_scale_stride = q_scale_stride;
+  p.kv_out = (uint16_t*)kv_out;
+  p.kv_out_stride = kv_out_stride;
+  p.status = status;
+  return cuda_status(fp8n::launch_mx(p, (cudaStream_t)stream));
+}
+
+fp8n_status fp8n_static_head_quant(const void* q, const void* k, const void* v,
+                                   int64_t qk_tok_stride, int64_t qk_head_stride,
+                                   int64_t v_tok_stride, int64_t v_head_stride, int64_t T,
+                                   int32_t H, int32_t Dqk, int32_t Dv, const float* q_descale,
+                                   const float* k_descale, const float* v_descale,
+                                   const int32_t* cu_seqlens, int32_t num_seqs, void* q_out,
+                                   void* k_out, void* v_out, uint32_t* status,
+                                   fp8n_stream_t stream) {
+  (void)cu_seqlens;
+  if (T < 0 || H < 1 || Dqk < 1 || Dv < 1 || num_seqs < 0) return FP8N_ERR_SHAPE;
+  if (Dqk % 8 || Dv % 8 || Dqk > 8192 || Dv > 8192 || H > 256) return FP8N_ERR_UNSUPPORTED;
+  if (qk_head_stride < Dqk || v_head_stride < Dv || qk_tok_stride < 0 || v_tok_stride < 0)
+    return FP8N_ERR_SHAPE;
+  // one launch addresses every chunk with 32-bit indices
+  const int64_t chunks = T * H * (int64_t)(2 * Dqk + Dv) / 8;
+  if (chunks >= (int64_t)1 << 31) return FP8N_ERR_UNSUPPORTED;
+  if (T == 0) return FP8N_OK;
+  if (!q || !k || !v || !q_descale || !k_descale || !v_descale || !q_out || !k_out || !v_out)
+    return FP8N_ERR_NULL;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(q_out) || !aligned16(k_out) ||
+      !aligned16(v_out) || qk_tok_stride % 8 || qk_head_stride % 8 || v_tok_stride % 8 ||
+      v_head_stride % 8 || ((uintptr_t)q_descale & 3u) || ((uintptr_t)k_descale & 3u) ||
+      ((uintptr_t)v_descale & 3u) || ((uintptr_t)status & 3u))
+    return FP8N_ERR_MISALIGNED;
+  fp8n::StaticParams p;
+  const void* in[3] = {q, k, v};
+  void* out[3] = {q_out, k_out, v_out};
+  const float* d[3] = {q_descale, k_descale, v_descale};
+  for (int i = 0; i < 3; ++i) {
+    p.t[i].x = (const uint16_t*)in[i];
+    p.t[i].tok_stride = i < 2 ? qk_tok_stride : v_tok_stride;
+    p.t[i].head_stride = i < 2 ? qk_head_stride : v_head_stride;
+    p.t[i].Dh = i < 2 ? Dqk : Dv;
+    p.t[i].descale = d[i];
+    p.t[i].out = (uint8_t*)out[i];
+  }
+  p.T = T;
+  p.H = H;
+  p.status = status;
+  return cuda_status(fp8n::launch_static(p, (cudaStream_t)stream));
+}
+
+fp8n_status fp8n_gate_act_bf16(const void* g, int64_t n, fp8n_act act, void* out,
+                               fp8n_stream_t stream) {
+  if (n < 0) return FP8N_ERR_SHAPE;
+  if (act != FP8N_ACT_SIGMOID && act != FP8N_ACT_SILU) return FP8N_ERR_UNSUPPORTED;
+  if (n == 0) return FP8N_OK;
+  if (!g || !out) return FP8N_ERR_NULL;
+  if (((uintptr_t)g & 1u) || ((uintptr_t)out & 1u)) return FP8N_ERR_MISALIGNED;
+  return cuda_status(fp8n::launch_gate_act((const uint16_t*)g, n, (int)act, (uint16_t*)out,
+                                           (cudaStream_t)stream));
+}
+
+fp8n_status fp8n_check_descales(const float* descale, int32_t n, fp8n_stream_t stream) {
+  if (n < 1 || n > 65536) return FP8N_ERR_SHAPE;
+  if (!descale) return FP8N_ERR_NULL;
+  if ((uintptr_t)descale & 3u) return FP8N_ERR_MISALIGNED;
+  std::vector<float> h((size_t)n);
+  cudaError_t e = cudaMemcpyAsync(h.data(), descale, sizeof(float) * (size_t)n,
+                                  cudaMemcpyDeviceToHost, (cudaStream_t)stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize((cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_status(e);
+  for (float x : h)
+    if (!(x > 0.0f) || std::isinf(x)) return FP8N_ERR_BAD_SCALE;
+  return FP8N_OK;
+}
+
+}  // extern "C"

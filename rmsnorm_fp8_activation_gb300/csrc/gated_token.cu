@@ -1,0 +1,344 @@
+// (A) Gated RMSNorm fused with per-token dynamic FP8 e4m3 quantisation.
+//
+// Source: "[ROCm][Kimi-K3] Fuse gated RMSNorm with per-token FP8 for KDA
+// o_proj" (vLLM PR 54254): one kernel for the gated norm and the per-token
+// amax quantisation; the torch reference helper rounds the normalised x to
+// the activation dtype, multiplies by the weight in that dtype and by
+// sigmoid(gate); the wrapper quantises the [t, heads*h] row with one scale.
+//
+// GB300 design: a persistent grid; each CTA walks tokens t = blockIdx.x,
+// blockIdx.x + gridDim.x, ...  The x and gate rows of a token (one contiguous
+// H*D bf16 span each) are staged into shared memory by cp.async.bulk copies
+// that complete on an mbarrier, NSTAGE tokens ahead.  Thread j of the CTA owns
+// 8*CPT consecutive elements of the row, so a head of D elements belongs to
+// TPH = D/(8*CPT) neighbouring lanes: its sum of squares is a Kahan sum per
+// thread and a double-float butterfly over those lanes.  y stays in registers
+// as bf16 pairs; the row amax needs one CTA barrier per token, after which the
+// stage is refilled and the codes are written with 8-byte stores.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace fp8n {
+namespace {
+
+constexpr int kHeader = 1024;  // mbarriers at 0, amax partials at 64
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
+                                         uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ float fmax_nan(float a, float b) {
+  float d;
+  asm("max.NaN.f32 %0, %1, %2;" : "=f"(d) : "f"(a), "f"(b));
+  return d;
+}
+
+// Slot of the thread's row segment read at step c: a rotation by j/(8/CPT)
+// makes the eight 16-byte reads of each quarter-warp hit distinct bank groups.
+template <int CPT>
+__device__ __forceinline__ int slot_of(int c, int j) {
+  return CPT == 1 ? 0 : (c + j / (8 / CPT)) % CPT;
+}
+
+// y pair = bf16(bf16(bf16(RN32(x*r)) * w) * bf16(act(g))) for one bf16 pair.
+template <int ACT>
+__device__ __forceinline__ uint32_t gated_pair(uint32_t xw, uint32_t gw, uint32_t ww, float r) {
+  uint32_t xn = pack_bf16x2(__fmul_rn(bf16_lo(xw), r), __fmul_rn(bf16_hi(xw), r));
+  return mul_bf16x2(mul_bf16x2(xn, ww), act_bf16_pair(gw, ACT));
+}
+
+// Codes of a y pair with the token scale (zero scale: signed zeros).
+__device__ __forceinline__ uint32_t quant_pair(uint32_t y, float scale, float rs, bool zero) {
+  float a = bf16_lo(y), b = bf16_hi(y);
+  if (!zero) {
+    a = div_rn(a, scale, rs);
+    b = div_rn(b, scale, rs);
+  }
+  return e4m3x2(a, b);
+}
+
+template <int ACT, int CPT, int TPH>
+__global__ void __launch_bounds__(512) gated_token_tma(const GatedParams p, int nstage) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const int row = p.H * p.D;
+  const uint32_t row_bytes = 2u * (uint32_t)row;
+  const uint32_t stage_bytes = 2u * row_bytes;
+  const int nthr = row / (8 * CPT);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
+  const bool active = tid < nthr;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
+  float* red = reinterpret_cast<float*>(smem + 64);
+  uint8_t* stages = smem + kHeader;
+
+  if (tid == 0) {
+    for (int s = 0; s < nstage; ++s) mbar_init(smem_u32(&bars[s]), 1);
+    asm volatile("fence.mbarrier_init.release.cluster;\n fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  __syncthreads();
+
+  auto issue = [&](int s, int64_t t) {
+    uint32_t bar = smem_u32(&bars[s]);
+    uint32_t dst = smem_u32(stages + (size_t)s * stage_bytes);
+    mbar_expect_tx(bar, stage_bytes);
+    bulk_g2s(dst, p.x + t * p.x_stride, row_bytes, bar);
+    bulk_g2s(dst + row_bytes, p.gate + t * p.gate_stride, row_bytes, bar);
+  };
+  if (tid == 0)
+    for (int s = 0; s < nstage; ++s) {
+      int64_t t = blockIdx.x + (int64_t)s * gridDim.x;
+      if (t < p.T) issue(s, t);
+    }
+
+  // This thread's weights, in the order its steps visit its slots.
+  uint4 wv[CPT];
+  const int seg = tid * 8 * CPT;  // first element of the thread's segment
+#pragma unroll
+  for (int c = 0; c < CPT; ++c) {
+    wv[c] = make_uint4(0, 0, 0, 0);
+    if (active)
+      wv[c] = *reinterpret_cast<const uint4*>(p.weight + (seg % p.D) + 8 * slot_of<CPT>(c, tid));
+  }
+  const float inv_d = 1.0f / (float)p.D;  // exact: D is a power of two here
+
+  int it = 0;
+  bool timeout = false;
+  for (int64_t t = blockIdx.x; t < p.T; t += gridDim.x, ++it) {
+    const int s = it % nstage;
+    if (!mbar_wait(smem_u32(&bars[s]), (uint32_t)(it / nstage) & 1u, kWaitLimit)) timeout = true;
+    const uint8_t* sx = stages + (size_t)s * stage_bytes + (size_t)seg * 2;
+    const uint8_t* sg = sx + row_bytes;
+
+    uint4 xr[CPT], gr[CPT];
+    kahan acc;
+#pragma unroll
+    for (int c = 0; c < CPT; ++c) {
+      xr[c] = gr[c] = make_uint4(0, 0, 0, 0);
+      if (active) {
+        const int off = 16 * slot_of<CPT>(c, tid);
+        xr[c] = *reinterpret_cast<const uint4*>(sx + off);
+        gr[c] = *reinterpret_cast<const uint4*>(sg + off);
+      }
+      const uint32_t* xw = &xr[c].x;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        acc.add_sq(bf16_lo(xw[k]));
+        acc.add_sq(bf16_hi(xw[k]));
+      }
+    }
+    df S = acc.value();
+#pragma unroll
+    for (int m = 1; m < TPH; m <<= 1) S = df_add(S, shfl_xor_df(S, m));
+    const float r = rms_factor(__fmul_rn(__fadd_rn(S.h, S.l), inv_d), p.eps);
+
+    uint32_t y[CPT][4];
+    uint32_t am2 = 0;
+#pragma unroll
+    for (int c = 0; c < CPT; ++c) {
+      const uint32_t *xw = &xr[c].x, *gw = &gr[c].x, *ww = &wv[c].x;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        y[c][k] = active ? gated_pair<ACT>(xw[k], gw[k], ww[k], r) : 0u;
+        am2 = absmax_bf16x2(am2, y[c][k]);
+      }
+    }
+    float amax = fmax_nan(bf16_lo(am2), bf16_hi(am2));
+#pragma unroll
+    for (int m = 16; m >= 1; m >>= 1) amax = fmax_nan(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, m));
+    float* redb = red + (it & 1) * 32;
+    if (lane == 0) redb[warp] = amax;
+    // every thread is done with stage s and has published its warp's amax
+    if (__syncthreads_or(timeout)) break;
+    if (tid == 0) {
+      const int64_t tn = t + (int64_t)nstage * gridDim.x;
+      if (tn < p.T) issue(s, tn);
+    }
+    float tam = redb[0];
+    for (int w = 1; w < nwarps; ++w) tam = fmax_nan(tam, redb[w]);
+    const float scale = __fdiv_rn(tam, 448.0f);
+    if (tid == 0) p.scale[t] = scale;
+    if (active) {
+      const float rs = __frcp_rn(scale);
+      const bool zero = (tam == 0.0f);
+      uint8_t* orow = p.out + t * p.out_stride + seg;
+#pragma unroll
+      for (int c = 0; c < CPT; ++c) {
+        uint2 o;
+        o.x = quant_pair(y[c][0], scale, rs, zero) | (quant_pair(y[c][1], scale, rs, zero) << 16);
+        o.y = quant_pair(y[c][2], scale, rs, zero) | (quant_pair(y[c][3], scale, rs, zero) << 16);
+        *reinterpret_cast<uint2*>(orow + 8 * slot_of<CPT>(c, tid)) = o;
+      }
+    }
+  }
+
+  if (timeout && tid == 0) {
+    if (p.status) atomicOr(p.status, kStatusTimeout);
+    // let copies still in flight land before the CTA's shared memory goes away
+    for (int i = it; i < it + nstage; ++i) {
+      const int64_t ti = blockIdx.x + (int64_t)i * gridDim.x;
+      if (ti < p.T) mbar_wait(smem_u32(&bars[i % nstage]), (uint32_t)(i / nstage) & 1u, kWaitLimit);
+    }
+  }
+}
+
+// Any D that is a multiple of 8: one CTA per token, three passes over the
+// (cache-resident) row: chunk sums of squares, then y and the amax, then y
+// again and the codes.  Used for head sizes the staged kernel does not take.
+template <int ACT>
+__global__ void __launch_bounds__(256) gated_token_generic(const GatedParams p) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const int row = p.H * p.D, nch = row / 8, cph = p.D / 8;
+  df* part = reinterpret_cast<df*>(smem);
+  float* rf = reinterpret_cast<float*>(smem + (size_t)nch * sizeof(df));
+  float* red = rf + p.H;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
+  const float n = (float)p.D;
+
+  for (int64_t t = blockIdx.x; t < p.T; t += gridDim.x) {
+    const uint16_t* xrow = p.x + t * p.x_stride;
+    const uint16_t* grow = p.gate + t * p.gate_stride;
+    for (int c = tid; c < nch; c += blockDim.x) {
+      const uint4 v = *reinterpret_cast<const uint4*>(xrow + 8 * c);
+      kahan acc;
+      const uint32_t* w = &v.x;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        acc.add_sq(bf16_lo(w[k]));
+        acc.add_sq(bf16_hi(w[k]));
+      }
+      part[c] = acc.value();
+    }
+    __syncthreads();
+    for (int h = warp; h < p.H; h += nwarps) {
+      df S = {0.0f, 0.0f};
+      for (int c = lane; c < cph; c += 32) S = df_add(S, part[h * cph + c]);
+#pragma unroll
+      for (int m = 16; m >= 1; m >>= 1) S = df_add(S, shfl_xor_df(S, m));
+      if (lane == 0) rf[h] = rms_factor(mean_from_sum(S, n, 0.0f, false), p.eps);
+    }
+    __syncthreads();
+
+    auto y_chunk = [&](int c, uint32_t y[4]) {
+      const uint4 xv = *reinterpret_cast<const uint4*>(xrow + 8 * c);
+      const uint4 gv = *reinterpret_cast<const uint4*>(grow + 8 * c);
+      const uint4 wv = *reinterpret_cast<const uint4*>(p.weight + 8 * (c % cph));
+      const float r = rf[c / cph];
+      const uint32_t *xw = &xv.x, *gw = &gv.x, *ww = &wv.x;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) y[k] = gated_pair<ACT>(xw[k], gw[k], ww[k], r);
+    };
+
+    uint32_t am2 = 0;
+    for (int c = tid; c < nch; c += blockDim.x) {
+      uint32_t y[4];
+      y_chunk(c, y);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) am2 = absmax_bf16x2(am2, y[k]);
+    }
+    float amax = fmax_nan(bf16_lo(am2), bf16_hi(am2));
+#pragma unroll
+    for (int m = 16; m >= 1; m >>= 1) amax = fmax_nan(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, m));
+    if (lane == 0) red[warp] = amax;
+    __syncthreads();
+    float tam = red[0];
+    for (int w = 1; w < nwarps; ++w) tam = fmax_nan(tam, red[w]);
+    const float scale = __fdiv_rn(tam, 448.0f);
+    const float rs = __frcp_rn(scale);
+    const bool zero = (tam == 0.0f);
+    if (tid == 0) p.scale[t] = scale;
+    uint8_t* orow = p.out + t * p.out_stride;
+    for (int c = tid; c < nch; c += blockDim.x) {
+      uint32_t y[4];
+      y_chunk(c, y);
+      uint2 o;
+      o.x = quant_pair(y[0], scale, rs, zero) | (quant_pair(y[1], scale, rs, zero) << 16);
+      o.y = quant_pair(y[2], scale, rs, zero) | (quant_pair(y[3], scale, rs, zero) << 16);
+      *reinterpret_cast<uint2*>(orow + 8 * c) = o;
+    }
+    __syncthreads();  // part / rf / red are reused by the next token
+  }
+}
+
+template <int ACT, int CPT, int TPH>
+cudaError_t launch_tma(const GatedParams& p, cudaStream_t stream) {
+  auto kern = gated_token_tma<ACT, CPT, TPH>;
+  const int row = p.H * p.D;
+  const int nthr = row / (8 * CPT);
+  const int block = (nthr + 31) / 32 * 32;
+  const size_t stage_bytes = 4u * (size_t)row;
+  int nstage = (int)((96 * 1024) / stage_bytes);
+  nstage = nstage < 2 ? 2 : (nstage > 4 ? 4 : nstage);
+  const size_t smem = kHeader + nstage * stage_bytes;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  int per_sm = 0;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, block, smem);
+  if (e != cudaSuccess) return e;
+  if (per_sm < 1) per_sm = 1;
+  const int64_t want = (int64_t)sm_count() * per_sm;
+  const int grid = (int)(p.T < want ? p.T : want);
+  kern<<<grid, block, smem, stream>>>(p, nstage);
+  return cudaGetLastError();
+}
+
+template <int ACT>
+cudaError_t launch_generic(const GatedParams& p, cudaStream_t stream) {
+  auto kern = gated_token_generic<ACT>;
+  const int row = p.H * p.D;
+  const size_t smem = (size_t)(row / 8) * sizeof(df) + (size_t)p.H * 4 + 32 * 4;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  int per_sm = 0;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 256, smem);
+  if (e != cudaSuccess) return e;
+  if (per_sm < 1) per_sm = 1;
+  const int64_t want = (int64_t)sm_count() * per_sm;
+  const int grid = (int)(p.T < want ? p.T : want);
+  kern<<<grid, 256, smem, stream>>>(p);
+  return cudaGetLastError();
+}
+
+template <int ACT>
+cudaError_t dispatch(const GatedParams& p, cudaStream_t stream) {
+  const int row = p.H * p.D;
+  // staged kernel: D/8 a power of two, a head spans at most a warp, the row
+  // fits one CTA and a stage fits shared memory
+  const int cpt = p.D >= 32 ? 4 : p.D / 8;
+  const int tph = p.D / (8 * cpt);
+  const bool pow2 = (p.D & (p.D - 1)) == 0;
+  if (pow2 && tph >= 1 && tph <= 32 && row / (8 * cpt) <= 512 && 4 * row <= 64 * 1024) {
+    switch (cpt * 100 + tph) {
+      case 101: return launch_tma<ACT, 1, 1>(p, stream);
+      case 201: return launch_tma<ACT, 2, 1>(p, stream);
+      case 401: return launch_tma<ACT, 4, 1>(p, stream);
+      case 402: return launch_tma<ACT, 4, 2>(p, stream);
+      case 404: return launch_tma<ACT, 4, 4>(p, stream);
+      case 408: return launch_tma<ACT, 4, 8>(p, stream);
+      case 416: return launch_tma<ACT, 4, 16>(p, stream);
+      case 432: return launch_tma<ACT, 4, 32>(p, stream);
+      default: break;
+    }
+  }
+  return launch_generic<ACT>(p, stream);
+}
+
+}  // namespace
+
+cudaError_t launch_gated(const GatedParams& p, cudaStream_t stream) {
+  return p.act == kActSilu ? dispatch<kActSilu>(p, stream) : dispatch<kActSigmoid>(p, stream);
+}
+
+}  // namespace fp8n

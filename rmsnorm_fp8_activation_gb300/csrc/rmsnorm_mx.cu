@@ -1,0 +1,201 @@
+// (B) Fused q/kv RMSNorm: q leaves as MXFP8 (E4M3 elements, one E8M0 scale
+// per 32 consecutive elements, scales row-major), kv as normalised bf16.
+//
+// Source: "[ROCm][Perf] FP8 o-projection for DeepSeek-V4.1-Flash MLA on AMD
+// MI355X" (vLLM PR 57081), third commit message: one producer normalises q
+// and kv and emits q as MXFP8 with row-major E8M0 scales, so the two q
+// consumers read the same quantised tensor.  Block scale rule: OCP
+// Microscaling Formats v1.0 section 5, X = 2^(floor(log2 amax) - 8) for E4M3.
+//
+// GB300 design: one warp per row, rows strided over a persistent grid.  Lane
+// l owns the 16-byte chunks l, l+32, l+64, ... of the q row and of the kv row
+// (coalesced 512-byte steps), kept in registers between the two passes (sum
+// of squares, then normalise + quantise).  An MX block is four consecutive
+// chunks, i.e. four neighbouring lanes of one step, so its amax takes two
+// xor-shuffles.  Rows longer than kResident steps are read twice instead.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace fp8n {
+namespace {
+
+constexpr int kResident = 8;  // register-resident 512-byte steps per tensor
+constexpr int kWarps = 8;
+
+__device__ __forceinline__ float fmax_nan(float a, float b) {
+  float d;
+  asm("max.NaN.f32 %0, %1, %2;" : "=f"(d) : "f"(a), "f"(b));
+  return d;
+}
+
+// bf16(bf16(RN32(x * r)) * w) for a chunk of 8 (4 pairs).
+__device__ __forceinline__ void norm_chunk(const uint4& xv, const uint4& wv, float r, uint32_t y[4]) {
+  const uint32_t *xw = &xv.x, *ww = &wv.x;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    uint32_t xn = pack_bf16x2(__fmul_rn(bf16_lo(xw[k]), r), __fmul_rn(bf16_hi(xw[k]), r));
+    y[k] = mul_bf16x2(xn, ww[k]);
+  }
+}
+
+// E8M0 exponent e (scale 2^e) of a block whose amax has bf16 bits A (>= 0):
+// floor(log2 A) - 8 clamped to [-127, 127]; -127 for a zero block; the code
+// 0xFF (returned as e = 128) for NaN or infinity.
+__device__ __forceinline__ int mx_exponent(uint32_t A) {
+  if (A >= 0x7F80u) return 128;
+  if (A == 0u) return -127;
+  const uint32_t ef = A >> 7;
+  const int E = ef ? (int)ef - 127 : -133 + (31 - __clz((int)(A & 0x7Fu)));
+  const int e = E - 8;
+  return e < -127 ? -127 : e;  // E <= 127, so e <= 119
+}
+
+template <bool RESIDENT>
+__global__ void __launch_bounds__(kWarps * 32) rmsnorm_mx_kernel(const MxParams p) {
+  const int lane = threadIdx.x & 31;
+  const int64_t gwarp = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5);
+  const int64_t nwarps = (int64_t)gridDim.x * kWarps;
+  const int qch = p.Nq / 8, kch = p.Nkv / 8;
+  const int qsteps = (qch + 31) / 32, ksteps = (kch + 31) / 32;
+  const bool q_pow2 = (p.Nq & (p.Nq - 1)) == 0, k_pow2 = (p.Nkv & (p.Nkv - 1)) == 0;
+
+  for (int64_t m = gwarp; m < p.M; m += nwarps) {
+    const uint16_t* qrow = p.q + m * p.q_stride;
+    const uint16_t* krow = p.kv + m * p.kv_stride;
+    uint4 qr[kResident], kr[kResident];
+    kahan aq, ak;
+#pragma unroll
+    for (int j = 0; j < kResident; ++j) {
+      qr[j] = kr[j] = make_uint4(0, 0, 0, 0);
+      if (RESIDENT) {
+        const int c = 32 * j + lane;
+        if (c < qch) qr[j] = *reinterpret_cast<const uint4*>(qrow + 8 * c);
+        if (c < kch) kr[j] = *reinterpret_cast<const uint4*>(krow + 8 * c);
+      }
+    }
+    if (RESIDENT) {
+#pragma unroll
+      for (int j = 0; j < kResident; ++j) {
+        const uint32_t *qw = &qr[j].x, *kw = &kr[j].x;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          aq.add_sq(bf16_lo(qw[k]));
+          aq.add_sq(bf16_hi(qw[k]));
+          ak.add_sq(bf16_lo(kw[k]));
+          ak.add_sq(bf16_hi(kw[k]));
+        }
+      }
+    } else {
+      for (int c = lane; c < qch; c += 32) {
+        const uint4 v = *reinterpret_cast<const uint4*>(qrow + 8 * c);
+        const uint32_t* w = &v.x;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          aq.add_sq(bf16_lo(w[k]));
+          aq.add_sq(bf16_hi(w[k]));
+        }
+      }
+      for (int c = lane; c < kch; c += 32) {
+        const uint4 v = *reinterpret_cast<const uint4*>(krow + 8 * c);
+        const uint32_t* w = &v.x;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          ak.add_sq(bf16_lo(w[k]));
+          ak.add_sq(bf16_hi(w[k]));
+        }
+      }
+    }
+    df Sq = aq.value(), Sk = ak.value();
+#pragma unroll
+    for (int s = 16; s >= 1; s >>= 1) {
+      Sq = df_add(Sq, shfl_xor_df(Sq, s));
+      Sk = df_add(Sk, shfl_xor_df(Sk, s));
+    }
+    const float rq = rms_factor(mean_from_sum(Sq, (float)p.Nq, 1.0f / (float)p.Nq, q_pow2), p.eps);
+    const float rk =
+        kch ? rms_factor(mean_from_sum(Sk, (float)p.Nkv, 1.0f / (float)p.Nkv, k_pow2), p.eps) : 0.0f;
+
+    uint8_t* qo = p.q_out + m * p.q_out_stride;
+    uint8_t* so = p.q_scale + m * p.q_scale_stride;
+    uint16_t* ko = p.kv_out + m * p.kv_out_stride;
+    // one 512-byte step of q: normalise, MX-quantise (all lanes take part in
+    // the block shuffles; lanes past the row end carry zeros)
+    auto q_step = [&](int j, const uint4& xv) {
+      const int c = 32 * j + lane;
+      uint4 wv = make_uint4(0, 0, 0, 0);
+      if (c < qch) wv = *reinterpret_cast<const uint4*>(p.q_weight + 8 * c);
+      uint32_t y[4];
+      norm_chunk(xv, wv, rq, y);
+      uint32_t am = absmax_bf16x2(absmax_bf16x2(y[0], y[1]), absmax_bf16x2(y[2], y[3]));
+      am = absmax_bf16x2(am, __shfl_xor_sync(0xFFFFFFFFu, am, 1));
+      am = absmax_bf16x2(am, __shfl_xor_sync(0xFFFFFFFFu, am, 2));
+      const uint32_t A = __float_as_uint(fmax_nan(bf16_lo(am), bf16_hi(am))) >> 16;
+      const int e = mx_exponent(A);
+      if (c < qch) {
+        if ((lane & 3) == 0) so[c >> 2] = (uint8_t)(e + 127);
+        uint2 o;
+        if (e == 128) {
+          o = make_uint2(0x7F7F7F7Fu, 0x7F7F7F7Fu);
+        } else {
+          const float sc = pow2i(-e);  // exact power-of-two scaling
+          uint32_t b[4];
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            b[k] = e4m3x2(__fmul_rn(bf16_lo(y[k]), sc), __fmul_rn(bf16_hi(y[k]), sc));
+          o = make_uint2(b[0] | (b[1] << 16), b[2] | (b[3] << 16));
+        }
+        *reinterpret_cast<uint2*>(qo + 8 * c) = o;
+      }
+    };
+    auto kv_step = [&](int j, const uint4& xv) {
+      const int c = 32 * j + lane;
+      if (c >= kch) return;
+      const uint4 wv = *reinterpret_cast<const uint4*>(p.kv_weight + 8 * c);
+      uint4 o;
+      norm_chunk(xv, wv, rk, &o.x);
+      *reinterpret_cast<uint4*>(ko + 8 * c) = o;
+    };
+    if (RESIDENT) {
+#pragma unroll
+      for (int j = 0; j < kResident; ++j)
+        if (j < qsteps) q_step(j, qr[j]);
+#pragma unroll
+      for (int j = 0; j < kResident; ++j)
+        if (j < ksteps) kv_step(j, kr[j]);
+    } else {
+      for (int j = 0; j < qsteps; ++j) {
+        const int c = 32 * j + lane;
+        uint4 xv = make_uint4(0, 0, 0, 0);
+        if (c < qch) xv = *reinterpret_cast<const uint4*>(qrow + 8 * c);
+        q_step(j, xv);
+      }
+      for (int j = 0; j < ksteps; ++j) {
+        const int c = 32 * j + lane;
+        uint4 xv = make_uint4(0, 0, 0, 0);
+        if (c < kch) xv = *reinterpret_cast<const uint4*>(krow + 8 * c);
+        kv_step(j, xv);
+      }
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_mx(const MxParams& p, cudaStream_t stream) {
+  const bool resident = p.Nq <= 256 * kResident && p.Nkv <= 256 * kResident;
+  const void* kern = resident ? (const void*)rmsnorm_mx_kernel<true> : (const void*)rmsnorm_mx_kernel<false>;
+  int per_sm = 0;
+  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kWarps * 32, 0);
+  if (e != cudaSuccess) return e;
+  if (per_sm < 1) per_sm = 1;
+  const int64_t want = (int64_t)sm_count() * per_sm;
+  const int64_t need = (p.M + kWarps - 1) / kWarps;
+  const int grid = (int)(need < want ? need : want);
+  if (resident)
+    rmsnorm_mx_kernel<true><<<grid, kWarps * 32, 0, stream>>>(p);
+  else
+    rmsnorm_mx_kernel<false><<<grid, kWarps * 32, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace fp8n
