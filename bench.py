@@ -1,0 +1,404 @@
+"""Benchmark of the normalize-then-quantize path on GB300.
+
+One step = one pass of the whole path over one batch of synthetic inputs,
+each operation at its largest workload, one launch each, in this order:
+  (B) fused q/kv RMSNorm + MXFP8      q [8192,1536], kv [8192,512]
+  (C) static per-head FP8 of Q/K/V    T = 151,153 packed tokens, H = 12, D 192/192/128
+  (A) gated RMSNorm + per-token FP8   x, gate [65536, 64, 128], sigmoid
+Metric: achieved HBM GB/s (algorithmic bytes: every input read once, every
+output written once) over the step, per kernel and in total; rows/s per kernel.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+For N > 1 run under torchrun: each rank runs the same per-GPU workload on its
+own GPU (weak scaling, no collective on the data path); rank 0 prints one JSON
+line with the max time over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+METRIC = "achieved HBM GB/s and % of GB300 peak per kernel; rows/s at 1 GPU vs CPU oracle"
+UNIT = "GB/s"
+WORKLOAD = ("step = rmsnorm_quant_mx q[8192,1536]+kv[8192,512] -> static_head_quant "
+            "Q,K[151153,12,192]+V[151153,12,128] -> gated_rmsnorm_quant_token "
+            "x,gate[65536,64,128] sigmoid; seed 0")
+# oracle samples (tokens of A, rows of B, tokens of C): about 10 s of one host
+# core for the CPU baseline, about 2 s per step for the reference arm
+CPU_SAMPLE = (4096, 8192, 16384)
+REF_SAMPLE = (512, 4096, 4096)
+L2_NOTE = ("inputs larger than L2: (A) 2.15 GB and (C) 2.61 GB per launch; the 55 MB of (B) "
+           "is evicted by the ~5 GB the other two kernels stream between its launches")
+
+
+def peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "source": "fallback"}
+
+
+def profiled_traffic(kernel_key: str):
+    """DRAM bytes per launch from a committed ncu summary, if the kernel's
+    sources are unchanged since the capture (else None)."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f).get(kernel_key)
+    if not d:
+        return None
+    h = hashlib.sha256()
+    for rel in d["sources"]:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    if h.hexdigest() != d["sources_sha256"]:
+        return None
+    return d["dram_bytes_per_launch"]
+
+
+class ClockSampler:
+    """nvidia-smi clocks/throttle sampling during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        import tempfile
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+# ---------------------------------------------------------------------------
+# workloads and their bytes
+# ---------------------------------------------------------------------------
+
+def make_inputs(rank: int, small: bool = False):
+    """Full workloads, or (small) the profiling case: 8192 tokens of the large
+    gated workload (268 MB of x + gate), the q/kv workload, and the first two
+    packed sequences of the static-head workload (more than L2 each)."""
+    import synth
+    W = synth.workloads(seed=rank)
+    wl, wm, ws = W["gated_large"], W["qkv_mx"], W["static_head"]
+    if small:
+        wl = synth.GatedWorkload("gated_large_8192", 8192, wl.H, wl.D, wl.act, wl.eps,
+                                 wl.outlier_p, wl.outlier_scale, wl.seed, wl.stream_base)
+        ws = synth.StaticHeadWorkload("static_head_2seq", seed=ws.seed, stream_base=ws.stream_base,
+                                      lengths=ws.lengths[:2])
+    inp = {"A": {"x": wl.x(), "gate": wl.gate(), "w": wl.weight(), "w_": wl},
+           "B": {"q": wm.q(), "kv": wm.kv(), "wq": wm.q_weight(), "wkv": wm.kv_weight(), "w_": wm}}
+    xs = {k: ws.tensor(k) for k in ("q", "k", "v")}
+    inp["C"] = {**xs, "d": ws.descales(xs), "cu": ws.cu_seqlens(), "w_": ws}
+    return inp
+
+
+def alg_bytes(inp) -> dict:
+    return {"A": inp["A"]["w_"].algorithmic_bytes(), "B": inp["B"]["w_"].algorithmic_bytes(),
+            "C": inp["C"]["w_"].algorithmic_bytes()}
+
+
+def rows(inp) -> dict:
+    return {"A": inp["A"]["w_"].T, "B": inp["B"]["w_"].M, "C": inp["C"]["w_"].T}
+
+
+# ---------------------------------------------------------------------------
+# the oracle on the host cores (CPU baseline and reference arm)
+# ---------------------------------------------------------------------------
+
+def oracle_sample(inp, n_a, n_b, n_c):
+    """Run the oracle on the first n tokens/rows of each workload; returns
+    (seconds, algorithmic bytes of the sample, description)."""
+    import oracle as O
+    a, b, c = inp["A"], inp["B"], inp["C"]
+    wl, wm, ws = a["w_"], b["w_"], c["w_"]
+    t0 = time.perf_counter()
+    O.gated_rmsnorm_quant_token(a["x"][:n_a], a["gate"][:n_a], a["w"], wl.eps, wl.act)
+    O.rmsnorm_quant_mx(b["q"][:n_b], b["wq"], b["kv"][:n_b], b["wkv"], wm.eps)
+    for k in ("q", "k", "v"):
+        O.static_head_quant(c[k][:n_c], c["d"][k])
+    dt = time.perf_counter() - t0
+    by = (n_a * wl.H * wl.D * 5 + n_b * (wm.Nq * 3 + wm.Nq // 32 + wm.Nkv * 4)
+          + n_c * ws.H * (2 * ws.Dqk + ws.Dv) * 3)
+    desc = ("first %d tokens of (A) gated_large, %d rows of (B) qkv_mx, %d tokens of (C) "
+            "static_head, single-threaded C oracle" % (n_a, n_b, n_c))
+    return dt, by, desc
+
+
+def reference_arm(args, rank: int, world: int) -> None:
+    """The oracle as it stands, on the host cores, on a bounded sample of the
+    same workload; rank 0 alone under torchrun."""
+    if rank != 0:
+        return
+    inp = make_inputs(0)
+    for _ in range(args.warmup):
+        oracle_sample(inp, *REF_SAMPLE)
+    dts, by, desc = [], 0, ""
+    for _ in range(args.steps):
+        dt, by, desc = oracle_sample(inp, *REF_SAMPLE)
+        dts.append(dt)
+    total = sum(dts)
+    value = by * args.steps / total / 1e9
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64+f32",
+            "data": "synthetic", "config": {"workload": WORKLOAD, "sample": desc},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "sample": desc},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+
+def ours(args, rank: int, world: int, local_rank: int) -> None:
+    import torch
+    import torch.distributed as dist
+
+    import rmsnorm_fp8_activation_gb300 as B
+    from rmsnorm_fp8_activation_gb300 import build as _build
+
+    _build.build()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    inp = make_inputs(rank, small=args.small)
+    nbytes = alg_bytes(inp)
+    nrows = rows(inp)
+
+    def d16(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
+
+    A, Bm, C = inp["A"], inp["B"], inp["C"]
+    wl, wm, ws = A["w_"], Bm["w_"], C["w_"]
+    g = {"x": d16(A["x"]), "gate": d16(A["gate"]), "w": d16(A["w"]),
+         "q": d16(Bm["q"]), "kv": d16(Bm["kv"]), "wq": d16(Bm["wq"]), "wkv": d16(Bm["wkv"]),
+         "Q": d16(C["q"]), "K": d16(C["k"]), "V": d16(C["v"]),
+         "dq": torch.from_numpy(C["d"]["q"]).to(dev), "dk": torch.from_numpy(C["d"]["k"]).to(dev),
+         "dv": torch.from_numpy(C["d"]["v"]).to(dev), "cu": torch.from_numpy(C["cu"]).to(dev)}
+    o = {"a": torch.empty((wl.T, wl.H * wl.D), dtype=torch.uint8, device=dev),
+         "as": torch.empty((wl.T,), dtype=torch.float32, device=dev),
+         "bq": torch.empty((wm.M, wm.Nq), dtype=torch.uint8, device=dev),
+         "bs": torch.empty((wm.M, wm.Nq // 32), dtype=torch.uint8, device=dev),
+         "bk": torch.empty((wm.M, wm.Nkv), dtype=torch.bfloat16, device=dev),
+         "cq": torch.empty(C["q"].shape, dtype=torch.uint8, device=dev),
+         "ck": torch.empty(C["k"].shape, dtype=torch.uint8, device=dev),
+         "cv": torch.empty(C["v"].shape, dtype=torch.uint8, device=dev)}
+    stream = torch.cuda.Stream(device=dev)
+
+    def step(ev=None):
+        if ev:
+            ev[0].record(stream)
+        B.fp8n_rmsnorm_quant_mx(g["q"], g["wq"], g["kv"], g["wkv"], wm.eps, q_out=o["bq"],
+                                q_scale=o["bs"], kv_out=o["bk"], stream=stream)
+        if ev:
+            ev[1].record(stream)
+        B.fp8n_static_head_quant(g["Q"], g["K"], g["V"], g["dq"], g["dk"], g["dv"],
+                                 cu_seqlens=g["cu"], q_out=o["cq"], k_out=o["ck"], v_out=o["cv"],
+                                 stream=stream)
+        if ev:
+            ev[2].record(stream)
+        B.fp8n_gated_rmsnorm_quant_token(g["x"], g["gate"], g["w"], wl.eps, wl.act, out=o["a"],
+                                         scale=o["as"], stream=stream)
+        if ev:
+            ev[3].record(stream)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step()
+    stream.synchronize()
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    time.sleep(0.3)
+    barrier()
+    torch.cuda.synchronize()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    with torch.cuda.stream(stream):
+        for k in range(args.steps):
+            step(evs[k])
+    t_end.record(stream)
+    stream.synchronize()
+    barrier()
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    total_ms = t_start.elapsed_time(t_end)
+    per = {"B": [], "C": [], "A": []}
+    for e in evs:
+        per["B"].append(e[0].elapsed_time(e[1]))
+        per["C"].append(e[1].elapsed_time(e[2]))
+        per["A"].append(e[2].elapsed_time(e[3]))
+    if args.small:  # profiling case: kernel times only, no bench line
+        if rank == 0:
+            print(json.dumps({"small": True, "ms_per_step": total_ms / args.steps,
+                              "avg_us": {k: 1e3 * statistics.mean(v) for k, v in per.items()},
+                              "alg_bytes": nbytes}), flush=True)
+        return
+
+    # end to end through the public API with host buffers: pinned inputs copied
+    # in, the three calls, the outputs copied back, every step
+    h_in = {k: v.cpu().pin_memory() for k, v in g.items()}
+    h_out = {k: torch.empty(v.shape, dtype=v.dtype).pin_memory() for k, v in o.items()}
+    h2d = sum(v.numel() * v.element_size() for v in h_in.values())
+    d2h = sum(v.numel() * v.element_size() for v in h_out.values())
+
+    def e2e_step():
+        for k in g:
+            g[k].copy_(h_in[k], non_blocking=True)
+        step()
+        for k in o:
+            h_out[k].copy_(o[k], non_blocking=True)
+
+    e2e_steps = max(3, min(args.steps, 10))
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            e2e_step()
+    stream.synchronize()
+    barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    with torch.cuda.stream(stream):
+        for _ in range(e2e_steps):
+            e2e_step()
+    e1.record(stream)
+    stream.synchronize()
+    barrier()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+
+    step_ms = total_ms / args.steps
+    if world > 1:
+        t = torch.tensor([step_ms, e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        step_ms, e2e_ms = float(t[0]), float(t[1])
+    if rank != 0:
+        return
+
+    total_bytes = sum(nbytes.values())
+    value = world * total_bytes / (step_ms * 1e-3) / 1e9
+    pk = peaks()
+    kernels = {}
+    names = {"A": "gated_rmsnorm_quant_token", "B": "rmsnorm_quant_mx", "C": "static_head_quant"}
+    for k in ("A", "B", "C"):
+        avg_ms = statistics.mean(per[k])
+        gbs = nbytes[k] / (avg_ms * 1e-3) / 1e9
+        kernels[names[k]] = {"avg_us": 1e3 * avg_ms, "alg_bytes": nbytes[k], "GB_s": gbs,
+                             "frac_of_peak": gbs / pk["hbm_gbs"],
+                             "rows_per_s": nrows[k] / (avg_ms * 1e-3)}
+    dom = max(kernels, key=lambda n: kernels[n]["avg_us"])
+    dom_key = {v: k for k, v in names.items()}[dom]
+    dom_ms = statistics.mean(per[dom_key])
+    ach = nbytes[dom_key] / (dom_ms * 1e-3) / 1e9
+
+    cpu_dt, cpu_by, cpu_desc = oracle_sample(inp, *CPU_SAMPLE)
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16->e4m3 (f32 arithmetic)", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "per_gpu_alg_bytes_per_step": total_bytes,
+                       "l2": L2_NOTE, "parallelism": "replicas" if world > 1 else "1 GPU"},
+            "roofline": {"bound": "hbm", "kernel": dom, "achieved": ach, "peak": pk["hbm_gbs"],
+                         "unit": "GB/s", "frac": ach / pk["hbm_gbs"],
+                         "peak_source": pk["source"] + " (MEASURED_PEAKS.json hbm_gbs)",
+                         "traffic": profiled_traffic(dom)},
+            "kernels": kernels,
+            "cpu_baseline": {"value": cpu_by / cpu_dt / 1e9, "unit": UNIT, "cores": 1,
+                             "kind": "oracle", "sample": cpu_desc,
+                             "seconds": cpu_dt},
+            "e2e": {"value": world * total_bytes / (e2e_ms * 1e-3) / 1e9, "unit": UNIT,
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "ms_per_step": e2e_ms},
+            "gpu_launches": 3 * args.steps,
+            "clocks": clk}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--small", action="store_true",
+                    help="profiling case (see make_inputs); prints kernel times only")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1 and args.impl == "ours":
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    if args.impl == "reference":
+        reference_arm(args, rank, world)
+    else:
+        ours(args, rank, world, local_rank)
+    if world > 1 and args.impl == "ours":
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -14,9 +14,10 @@
  * round-to-nearest-even to bfloat16, "e4m3()" saturating round-to-nearest-even
  * to E4M3 (|v| >= 448 -> +-448, sign of zero kept).
  *
- * Alignment: every tensor pointer must be 16-byte aligned, and every row
- * stride must keep rows 16-byte aligned (a multiple of 8 bf16 elements, of 16
- * e4m3 / E8M0 bytes for the MX q output and scale rows; see each call).
+ * Alignment: every tensor pointer must be 16-byte aligned; bf16 row strides
+ * must be multiples of 8 elements (16-byte rows) and e4m3 row strides
+ * multiples of 8 bytes (the kernels move 16-byte input and 8-byte output
+ * chunks); see each call.
  *
  * Errors: a nonzero fp8n_status is returned and nothing is enqueued when an
  * argument is invalid.  FP8N_ERR_CUDA means a CUDA call failed; the CUDA error
@@ -85,7 +86,7 @@ uint32_t fp8n_version(void);
  *           x_stride / gate_stride (elements, multiples of 8, >= H*D).
  * weight  : bf16 [D], shared by all heads.
  * out     : e4m3 [T, H*D], token stride out_stride (bytes = elements,
- *           multiple of 16, >= H*D).
+ *           multiple of 8, >= H*D).
  * scale   : fp32 [T].
  * Limits  : D a multiple of 8, 8 <= D <= 8192, H >= 1, H*D <= 16384,
  *           eps finite and >= 0; otherwise FP8N_ERR_UNSUPPORTED / _SHAPE.
@@ -114,7 +115,7 @@ fp8n_status fp8n_gated_rmsnorm_quant_token(const void* x, int64_t x_stride, cons
  * q     : bf16 [M, Nq], row stride q_stride (elements, multiple of 8).
  * kv    : bf16 [M, Nkv], row stride kv_stride (elements, multiple of 8); may be
  *         NULL when Nkv == 0.
- * q_out : e4m3 [M, Nq], row stride q_out_stride (bytes, multiple of 16).
+ * q_out : e4m3 [M, Nq], row stride q_out_stride (bytes, multiple of 8).
  * q_scale: E8M0 uint8 [M, Nq/32] row-major, row stride q_scale_stride (bytes).
  * kv_out: bf16 [M, Nkv], row stride kv_out_stride (elements, multiple of 8).
  * Limits: Nq a multiple of 32 with 32 <= Nq <= 16384; Nkv a multiple of 8 with

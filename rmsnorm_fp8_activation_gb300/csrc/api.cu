@@ -65,7 +65,7 @@ fp8n_status fp8n_gated_rmsnorm_quant_token(const void* x, int64_t x_stride, cons
   if (T == 0) return FP8N_OK;
   if (!x || !gate || !weight || !out || !scale) return FP8N_ERR_NULL;
   if (!aligned16(x) || !aligned16(gate) || !aligned16(weight) || !aligned16(out) ||
-      x_stride % 8 || gate_stride % 8 || out_stride % 16 || ((uintptr_t)scale & 3u) ||
+      x_stride % 8 || gate_stride % 8 || out_stride % 8 || ((uintptr_t)scale & 3u) ||
       ((uintptr_t)status & 3u))
     return FP8N_ERR_MISALIGNED;
   fp8n::GatedParams p;
@@ -101,7 +101,7 @@ fp8n_status fp8n_rmsnorm_quant_mx(const void* q, int64_t q_stride, const void* q
   if (!q || !q_weight || !q_out || !q_scale) return FP8N_ERR_NULL;
   if (Nkv > 0 && (!kv || !kv_weight || !kv_out)) return FP8N_ERR_NULL;
   if (!aligned16(q) || !aligned16(q_weight) || !aligned16(q_out) || q_stride % 8 ||
-      q_out_stride % 16 || ((uintptr_t)status & 3u))
+      q_out_stride % 8 || ((uintptr_t)status & 3u))
     return FP8N_ERR_MISALIGNED;
   if (Nkv > 0 && (!aligned16(kv) || !aligned16(kv_weight) || !aligned16(kv_out) ||
                   kv_stride % 8 || kv_out_stride % 8))

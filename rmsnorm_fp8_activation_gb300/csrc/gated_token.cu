@@ -61,15 +61,38 @@ __device__ __forceinline__ uint32_t gated_pair(uint32_t xw, uint32_t gw, uint32_
   return mul_bf16x2(mul_bf16x2(xn, ww), act_bf16_pair(gw, ACT));
 }
 
-// Codes of a y pair with the token scale (zero scale: signed zeros).
-__device__ __forceinline__ uint32_t quant_pair(uint32_t y, float scale, float rs, bool zero) {
-  float a = bf16_lo(y), b = bf16_hi(y);
-  if (!zero) {
-    a = div_rn(a, scale, rs);
-    b = div_rn(b, scale, rs);
+// Token quantiser: code = e4m3(RN32(y / scale)).  A zero scale gives signed
+// zero codes.  A scale below 2^-126 (all |y| tiny) has no finite binary32
+// reciprocal, so y and the scale are both multiplied by 2^64 first (exact
+// power-of-two scalings that leave the quotient unchanged).
+struct TokenQuant {
+  float scale, rs, ymul;
+  bool zero, tiny;
+  __device__ __forceinline__ TokenQuant(float s) {
+    zero = (s == 0.0f);
+    tiny = (s > 0.0f) && (s < 0x1p-126f);
+    scale = tiny ? __fmul_rn(s, 0x1p64f) : s;
+    ymul = 0x1p64f;
+    rs = __frcp_rn(scale);
   }
-  return e4m3x2(a, b);
-}
+  // The quotient takes the sign of y: the FMA correction of div_rn turns
+  // -0/scale into +0, and the scale is positive.
+  template <bool TINY>
+  __device__ __forceinline__ uint32_t pair(uint32_t y) const {
+    float a = bf16_lo(y), b = bf16_hi(y);
+    if (!zero) {
+      const float a2 = TINY ? __fmul_rn(a, ymul) : a, b2 = TINY ? __fmul_rn(b, ymul) : b;
+      a = copysignf(div_rn(a2, scale, rs), a);
+      b = copysignf(div_rn(b2, scale, rs), b);
+    }
+    return e4m3x2(a, b);
+  }
+  template <bool TINY>
+  __device__ __forceinline__ uint2 chunk(const uint32_t y[4]) const {
+    return make_uint2(pair<TINY>(y[0]) | (pair<TINY>(y[1]) << 16),
+                      pair<TINY>(y[2]) | (pair<TINY>(y[3]) << 16));
+  }
+};
 
 template <int ACT, int CPT, int TPH>
 __global__ void __launch_bounds__(512) gated_token_tma(const GatedParams p, int nstage) {
@@ -171,15 +194,16 @@ __global__ void __launch_bounds__(512) gated_token_tma(const GatedParams p, int 
     const float scale = __fdiv_rn(tam, 448.0f);
     if (tid == 0) p.scale[t] = scale;
     if (active) {
-      const float rs = __frcp_rn(scale);
-      const bool zero = (tam == 0.0f);
+      const TokenQuant tq(scale);
       uint8_t* orow = p.out + t * p.out_stride + seg;
+      if (!tq.tiny) {
 #pragma unroll
-      for (int c = 0; c < CPT; ++c) {
-        uint2 o;
-        o.x = quant_pair(y[c][0], scale, rs, zero) | (quant_pair(y[c][1], scale, rs, zero) << 16);
-        o.y = quant_pair(y[c][2], scale, rs, zero) | (quant_pair(y[c][3], scale, rs, zero) << 16);
-        *reinterpret_cast<uint2*>(orow + 8 * slot_of<CPT>(c, tid)) = o;
+        for (int c = 0; c < CPT; ++c)
+          *reinterpret_cast<uint2*>(orow + 8 * slot_of<CPT>(c, tid)) = tq.chunk<false>(y[c]);
+      } else {
+#pragma unroll
+        for (int c = 0; c < CPT; ++c)
+          *reinterpret_cast<uint2*>(orow + 8 * slot_of<CPT>(c, tid)) = tq.chunk<true>(y[c]);
       }
     }
   }
@@ -256,17 +280,13 @@ __global__ void __launch_bounds__(256) gated_token_generic(const GatedParams p) 
     float tam = red[0];
     for (int w = 1; w < nwarps; ++w) tam = fmax_nan(tam, red[w]);
     const float scale = __fdiv_rn(tam, 448.0f);
-    const float rs = __frcp_rn(scale);
-    const bool zero = (tam == 0.0f);
+    const TokenQuant tq(scale);
     if (tid == 0) p.scale[t] = scale;
     uint8_t* orow = p.out + t * p.out_stride;
     for (int c = tid; c < nch; c += blockDim.x) {
       uint32_t y[4];
       y_chunk(c, y);
-      uint2 o;
-      o.x = quant_pair(y[0], scale, rs, zero) | (quant_pair(y[1], scale, rs, zero) << 16);
-      o.y = quant_pair(y[2], scale, rs, zero) | (quant_pair(y[3], scale, rs, zero) << 16);
-      *reinterpret_cast<uint2*>(orow + 8 * c) = o;
+      *reinterpret_cast<uint2*>(orow + 8 * c) = tq.tiny ? tq.chunk<true>(y) : tq.chunk<false>(y);
     }
     __syncthreads();  // part / rf / red are reused by the next token
   }

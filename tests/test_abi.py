@@ -73,7 +73,7 @@ def test_gated_validation(L):
     assert gated(L, sc=None) == NULL
     assert gated(L, x=P16 + 8) == MISALIGNED
     assert gated(L, xs=4100) == MISALIGNED
-    assert gated(L, os=4104) == MISALIGNED
+    assert gated(L, os=4100) == MISALIGNED
 
 
 def mx(L, **kw):
