@@ -122,6 +122,26 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------------------
+# multi-rank bookkeeping (replicas: no collective on the data path)
+# ---------------------------------------------------------------------------
+
+def reduce_max(values, world: int, device="cpu"):
+    """Element-wise max of per-rank timings over all ranks (every rank gets it)."""
+    if world <= 1:
+        return [float(v) for v in values]
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.tolist()]
+
+
+def aggregate_gbs(bytes_per_rank: int, world: int, ms: float) -> float:
+    """Whole-job GB/s: the bytes all ranks processed over the slowest rank's time."""
+    return world * bytes_per_rank / (ms * 1e-3) / 1e9
+
+
+# ---------------------------------------------------------------------------
 # workloads and their bytes
 # ---------------------------------------------------------------------------
 
@@ -326,16 +346,12 @@ def ours(args, rank: int, world: int, local_rank: int) -> None:
     barrier()
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
 
-    step_ms = total_ms / args.steps
-    if world > 1:
-        t = torch.tensor([step_ms, e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        step_ms, e2e_ms = float(t[0]), float(t[1])
+    step_ms, e2e_ms = reduce_max([total_ms / args.steps, e2e_ms], world, dev)
     if rank != 0:
         return
 
     total_bytes = sum(nbytes.values())
-    value = world * total_bytes / (step_ms * 1e-3) / 1e9
+    value = aggregate_gbs(total_bytes, world, step_ms)
     pk = peaks()
     kernels = {}
     names = {"A": "gated_rmsnorm_quant_token", "B": "rmsnorm_quant_mx", "C": "static_head_quant"}
@@ -365,7 +381,7 @@ def ours(args, rank: int, world: int, local_rank: int) -> None:
             "cpu_baseline": {"value": cpu_by / cpu_dt / 1e9, "unit": UNIT, "cores": 1,
                              "kind": "oracle", "sample": cpu_desc,
                              "seconds": cpu_dt},
-            "e2e": {"value": world * total_bytes / (e2e_ms * 1e-3) / 1e9, "unit": UNIT,
+            "e2e": {"value": aggregate_gbs(total_bytes, world, e2e_ms), "unit": UNIT,
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "ms_per_step": e2e_ms},
             "gpu_launches": 3 * args.steps,
@@ -376,8 +392,8 @@ def ours(args, rank: int, world: int, local_rank: int) -> None:
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=500)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--small", action="store_true",
                     help="profiling case (see make_inputs); prints kernel times only")

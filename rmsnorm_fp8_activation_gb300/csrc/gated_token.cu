@@ -23,6 +23,14 @@ namespace {
 
 constexpr int kHeader = 1024;  // mbarriers at 0, amax partials at 64
 
+// RN32(amax / 448) for amax >= 0: the Markstein sequence with the constant
+// RN(1/448) gives the IEEE quotient for every finite bf16 amax (checked
+// exhaustively on the host); infinities and NaN take the plain division.
+__device__ __forceinline__ float scale_of(float amax) {
+  if (!(amax <= 3.402823466e38f)) return __fdiv_rn(amax, 448.0f);
+  return div_rn(amax, 448.0f, 1.0f / 448.0f);
+}
+
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
 }
@@ -54,38 +62,44 @@ __device__ __forceinline__ int slot_of(int c, int j) {
   return CPT == 1 ? 0 : (c + j / (8 / CPT)) % CPT;
 }
 
-// y pair = bf16(bf16(bf16(RN32(x*r)) * w) * bf16(act(g))) for one bf16 pair.
-template <int ACT>
-__device__ __forceinline__ uint32_t gated_pair(uint32_t xw, uint32_t gw, uint32_t ww, float r) {
-  uint32_t xn = pack_bf16x2(__fmul_rn(bf16_lo(xw), r), __fmul_rn(bf16_hi(xw), r));
-  return mul_bf16x2(mul_bf16x2(xn, ww), act_bf16_pair(gw, ACT));
+// y pair = bf16(bf16(bf16(RN32(x*r)) * w) * ga) for one bf16 pair, where ga
+// is the bf16 pair bf16(act(g)).
+__device__ __forceinline__ uint32_t gated_pair(uint32_t xw, uint32_t ga, uint32_t ww, f2_t r2) {
+  const uint32_t xn = f2_to_bf2(mul2(bf2_to_f2(xw), r2));
+  return mul_bf16x2(mul_bf16x2(xn, ww), ga);
 }
 
-// Token quantiser: code = e4m3(RN32(y / scale)).  A zero scale gives signed
-// zero codes.  A scale below 2^-126 (all |y| tiny) has no finite binary32
-// reciprocal, so y and the scale are both multiplied by 2^64 first (exact
-// power-of-two scalings that leave the quotient unchanged).
+// Running max of |y| over bf16 pairs (NaN-propagating); acc stays >= 0.
+__device__ __forceinline__ uint32_t amax_step(uint32_t acc, uint32_t y) {
+  uint32_t d;
+  asm("max.NaN.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(acc), "r"(y & 0x7FFF7FFFu));
+  return d;
+}
+
+// Token quantiser: code = e4m3(RN32(y / scale)), from the correctly rounded
+// reciprocal and one FMA correction on packed pairs.  It is arranged on -y
+// (q0 = (-y)*(-1/s), e = q0*s - y, q = q0 - e/s) so that the signs of zero
+// quotients survive.  A zero scale gives signed zero codes.  A scale below
+// 2^-126 (all |y| tiny) has no finite binary32 reciprocal, so y and the scale
+// are both multiplied by 2^64 first: exact scalings that keep the quotient.
 struct TokenQuant {
-  float scale, rs, ymul;
+  f2_t s2, nrs2;
   bool zero, tiny;
   __device__ __forceinline__ TokenQuant(float s) {
     zero = (s == 0.0f);
     tiny = (s > 0.0f) && (s < 0x1p-126f);
-    scale = tiny ? __fmul_rn(s, 0x1p64f) : s;
-    ymul = 0x1p64f;
-    rs = __frcp_rn(scale);
+    const float sc = tiny ? __fmul_rn(s, 0x1p64f) : s;
+    s2 = splat2(sc);
+    nrs2 = splat2(-__frcp_rn(sc));
   }
-  // The quotient takes the sign of y: the FMA correction of div_rn turns
-  // -0/scale into +0, and the scale is positive.
   template <bool TINY>
   __device__ __forceinline__ uint32_t pair(uint32_t y) const {
-    float a = bf16_lo(y), b = bf16_hi(y);
-    if (!zero) {
-      const float a2 = TINY ? __fmul_rn(a, ymul) : a, b2 = TINY ? __fmul_rn(b, ymul) : b;
-      a = copysignf(div_rn(a2, scale, rs), a);
-      b = copysignf(div_rn(b2, scale, rs), b);
-    }
-    return e4m3x2(a, b);
+    if (zero) return f2_to_e4m3x2(bf2_to_f2(y));
+    f2_t ny = bf2_to_f2(y ^ 0x80008000u);
+    if (TINY) ny = mul2(ny, splat2(0x1p64f));
+    const f2_t q0 = mul2(ny, nrs2);
+    const f2_t e = fma2(q0, s2, ny);
+    return f2_to_e4m3x2(fma2(e, nrs2, q0));
   }
   template <bool TINY>
   __device__ __forceinline__ uint2 chunk(const uint32_t y[4]) const {
@@ -105,8 +119,11 @@ __global__ void __launch_bounds__(512) gated_token_tma(const GatedParams p, int 
   const bool active = tid < nthr;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
   float* red = reinterpret_cast<float*>(smem + 64);
-  uint8_t* stages = smem + kHeader;
+  uint16_t* wsm = reinterpret_cast<uint16_t*>(smem + kHeader);  // weight [D]
+  uint8_t* stages = smem + kHeader + 2 * p.D;
 
+  for (int i = tid; i < p.D / 8; i += blockDim.x)
+    reinterpret_cast<uint4*>(wsm)[i] = reinterpret_cast<const uint4*>(p.weight)[i];
   if (tid == 0) {
     for (int s = 0; s < nstage; ++s) mbar_init(smem_u32(&bars[s]), 1);
     asm volatile("fence.mbarrier_init.release.cluster;\n fence.proxy.async.shared::cta;" ::: "memory");
@@ -126,15 +143,8 @@ __global__ void __launch_bounds__(512) gated_token_tma(const GatedParams p, int 
       if (t < p.T) issue(s, t);
     }
 
-  // This thread's weights, in the order its steps visit its slots.
-  uint4 wv[CPT];
   const int seg = tid * 8 * CPT;  // first element of the thread's segment
-#pragma unroll
-  for (int c = 0; c < CPT; ++c) {
-    wv[c] = make_uint4(0, 0, 0, 0);
-    if (active)
-      wv[c] = *reinterpret_cast<const uint4*>(p.weight + (seg % p.D) + 8 * slot_of<CPT>(c, tid));
-  }
+  const uint16_t* wseg = wsm + (seg % p.D);
   const float inv_d = 1.0f / (float)p.D;  // exact: D is a power of two here
 
   int it = 0;
@@ -145,37 +155,43 @@ __global__ void __launch_bounds__(512) gated_token_tma(const GatedParams p, int 
     const uint8_t* sx = stages + (size_t)s * stage_bytes + (size_t)seg * 2;
     const uint8_t* sg = sx + row_bytes;
 
-    uint4 xr[CPT], gr[CPT];
-    kahan acc;
+    uint4 xr[CPT], ga[CPT];
+    kahan2 acc;
 #pragma unroll
     for (int c = 0; c < CPT; ++c) {
-      xr[c] = gr[c] = make_uint4(0, 0, 0, 0);
+      xr[c] = ga[c] = make_uint4(0, 0, 0, 0);
       if (active) {
         const int off = 16 * slot_of<CPT>(c, tid);
         xr[c] = *reinterpret_cast<const uint4*>(sx + off);
-        gr[c] = *reinterpret_cast<const uint4*>(sg + off);
+        ga[c] = *reinterpret_cast<const uint4*>(sg + off);
       }
       const uint32_t* xw = &xr[c].x;
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        acc.add_sq(bf16_lo(xw[k]));
-        acc.add_sq(bf16_hi(xw[k]));
-      }
+      for (int k = 0; k < 4; ++k) acc.add_sq(xw[k]);
+    }
+    // the gate factors do not depend on the norm: computed while the sums
+    // reduce (inactive lanes hold zero gates, which are cheap and unused)
+#pragma unroll
+    for (int c = 0; c < CPT; ++c) {
+      uint32_t* gw = &ga[c].x;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) gw[k] = act_bf16_pair(gw[k], ACT);
     }
     df S = acc.value();
 #pragma unroll
     for (int m = 1; m < TPH; m <<= 1) S = df_add(S, shfl_xor_df(S, m));
-    const float r = rms_factor(__fmul_rn(__fadd_rn(S.h, S.l), inv_d), p.eps);
+    const f2_t r2 = splat2(rms_factor(__fmul_rn(__fadd_rn(S.h, S.l), inv_d), p.eps));
 
     uint32_t y[CPT][4];
     uint32_t am2 = 0;
 #pragma unroll
     for (int c = 0; c < CPT; ++c) {
-      const uint32_t *xw = &xr[c].x, *gw = &gr[c].x, *ww = &wv[c].x;
+      const uint4 wv = *reinterpret_cast<const uint4*>(wseg + 8 * slot_of<CPT>(c, tid));
+      const uint32_t *xw = &xr[c].x, *gw = &ga[c].x, *ww = &wv.x;
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
-        y[c][k] = active ? gated_pair<ACT>(xw[k], gw[k], ww[k], r) : 0u;
-        am2 = absmax_bf16x2(am2, y[c][k]);
+        y[c][k] = gated_pair(xw[k], gw[k], ww[k], r2);
+        am2 = amax_step(am2, y[c][k]);
       }
     }
     float amax = fmax_nan(bf16_lo(am2), bf16_hi(am2));
@@ -191,7 +207,7 @@ __global__ void __launch_bounds__(512) gated_token_tma(const GatedParams p, int 
     }
     float tam = redb[0];
     for (int w = 1; w < nwarps; ++w) tam = fmax_nan(tam, redb[w]);
-    const float scale = __fdiv_rn(tam, 448.0f);
+    const float scale = scale_of(tam);
     if (tid == 0) p.scale[t] = scale;
     if (active) {
       const TokenQuant tq(scale);
@@ -236,13 +252,10 @@ __global__ void __launch_bounds__(256) gated_token_generic(const GatedParams p) 
     const uint16_t* grow = p.gate + t * p.gate_stride;
     for (int c = tid; c < nch; c += blockDim.x) {
       const uint4 v = *reinterpret_cast<const uint4*>(xrow + 8 * c);
-      kahan acc;
+      kahan2 acc;
       const uint32_t* w = &v.x;
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        acc.add_sq(bf16_lo(w[k]));
-        acc.add_sq(bf16_hi(w[k]));
-      }
+      for (int k = 0; k < 4; ++k) acc.add_sq(w[k]);
       part[c] = acc.value();
     }
     __syncthreads();
@@ -259,10 +272,10 @@ __global__ void __launch_bounds__(256) gated_token_generic(const GatedParams p) 
       const uint4 xv = *reinterpret_cast<const uint4*>(xrow + 8 * c);
       const uint4 gv = *reinterpret_cast<const uint4*>(grow + 8 * c);
       const uint4 wv = *reinterpret_cast<const uint4*>(p.weight + 8 * (c % cph));
-      const float r = rf[c / cph];
+      const f2_t r2 = splat2(rf[c / cph]);
       const uint32_t *xw = &xv.x, *gw = &gv.x, *ww = &wv.x;
 #pragma unroll
-      for (int k = 0; k < 4; ++k) y[k] = gated_pair<ACT>(xw[k], gw[k], ww[k], r);
+      for (int k = 0; k < 4; ++k) y[k] = gated_pair(xw[k], act_bf16_pair(gw[k], ACT), ww[k], r2);
     };
 
     uint32_t am2 = 0;
@@ -270,7 +283,7 @@ __global__ void __launch_bounds__(256) gated_token_generic(const GatedParams p) 
       uint32_t y[4];
       y_chunk(c, y);
 #pragma unroll
-      for (int k = 0; k < 4; ++k) am2 = absmax_bf16x2(am2, y[k]);
+      for (int k = 0; k < 4; ++k) am2 = amax_step(am2, y[k]);
     }
     float amax = fmax_nan(bf16_lo(am2), bf16_hi(am2));
 #pragma unroll
@@ -279,7 +292,7 @@ __global__ void __launch_bounds__(256) gated_token_generic(const GatedParams p) 
     __syncthreads();
     float tam = red[0];
     for (int w = 1; w < nwarps; ++w) tam = fmax_nan(tam, red[w]);
-    const float scale = __fdiv_rn(tam, 448.0f);
+    const float scale = scale_of(tam);
     const TokenQuant tq(scale);
     if (tid == 0) p.scale[t] = scale;
     uint8_t* orow = p.out + t * p.out_stride;
@@ -301,7 +314,7 @@ cudaError_t launch_tma(const GatedParams& p, cudaStream_t stream) {
   const size_t stage_bytes = 4u * (size_t)row;
   int nstage = (int)((96 * 1024) / stage_bytes);
   nstage = nstage < 2 ? 2 : (nstage > 4 ? 4 : nstage);
-  const size_t smem = kHeader + nstage * stage_bytes;
+  const size_t smem = kHeader + 2 * (size_t)p.D + nstage * stage_bytes;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   int per_sm = 0;

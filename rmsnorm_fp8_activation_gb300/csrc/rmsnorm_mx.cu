@@ -12,14 +12,13 @@
 // (coalesced 512-byte steps), kept in registers between the two passes (sum
 // of squares, then normalise + quantise).  An MX block is four consecutive
 // chunks, i.e. four neighbouring lanes of one step, so its amax takes two
-// xor-shuffles.  Rows longer than kResident steps are read twice instead.
+// xor-shuffles.  Rows longer than eight steps are read twice instead.
 #include "common.cuh"
 #include "kernels.h"
 
 namespace fp8n {
 namespace {
 
-constexpr int kResident = 8;  // register-resident 512-byte steps per tensor
 constexpr int kWarps = 8;
 
 __device__ __forceinline__ float fmax_nan(float a, float b) {
@@ -29,13 +28,10 @@ __device__ __forceinline__ float fmax_nan(float a, float b) {
 }
 
 // bf16(bf16(RN32(x * r)) * w) for a chunk of 8 (4 pairs).
-__device__ __forceinline__ void norm_chunk(const uint4& xv, const uint4& wv, float r, uint32_t y[4]) {
+__device__ __forceinline__ void norm_chunk(const uint4& xv, const uint4& wv, f2_t r2, uint32_t y[4]) {
   const uint32_t *xw = &xv.x, *ww = &wv.x;
 #pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    uint32_t xn = pack_bf16x2(__fmul_rn(bf16_lo(xw[k]), r), __fmul_rn(bf16_hi(xw[k]), r));
-    y[k] = mul_bf16x2(xn, ww[k]);
-  }
+  for (int k = 0; k < 4; ++k) y[k] = mul_bf16x2(f2_to_bf2(mul2(bf2_to_f2(xw[k]), r2)), ww[k]);
 }
 
 // E8M0 exponent e (scale 2^e) of a block whose amax has bf16 bits A (>= 0):
@@ -50,8 +46,11 @@ __device__ __forceinline__ int mx_exponent(uint32_t A) {
   return e < -127 ? -127 : e;  // E <= 127, so e <= 119
 }
 
-template <bool RESIDENT>
-__global__ void __launch_bounds__(kWarps * 32) rmsnorm_mx_kernel(const MxParams p) {
+// QS / KS: 512-byte steps of the q / kv row held in registers between the two
+// passes (0: the row is read again in the second pass).
+template <int QS, int KS>
+__global__ void __launch_bounds__(kWarps * 32, (QS + KS >= 8) ? 2 : 3) rmsnorm_mx_kernel(const MxParams p) {
+  constexpr bool RESIDENT = QS > 0;
   const int lane = threadIdx.x & 31;
   const int64_t gwarp = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5);
   const int64_t nwarps = (int64_t)gridDim.x * kWarps;
@@ -62,47 +61,46 @@ __global__ void __launch_bounds__(kWarps * 32) rmsnorm_mx_kernel(const MxParams 
   for (int64_t m = gwarp; m < p.M; m += nwarps) {
     const uint16_t* qrow = p.q + m * p.q_stride;
     const uint16_t* krow = p.kv + m * p.kv_stride;
-    uint4 qr[kResident], kr[kResident];
-    kahan aq, ak;
-#pragma unroll
-    for (int j = 0; j < kResident; ++j) {
-      qr[j] = kr[j] = make_uint4(0, 0, 0, 0);
-      if (RESIDENT) {
-        const int c = 32 * j + lane;
-        if (c < qch) qr[j] = *reinterpret_cast<const uint4*>(qrow + 8 * c);
-        if (c < kch) kr[j] = *reinterpret_cast<const uint4*>(krow + 8 * c);
-      }
-    }
+    constexpr int QR = QS > 0 ? QS : 1, KR = KS > 0 ? KS : 1;
+    uint4 qr[QR], kr[KR];
+    kahan2 aq, ak;
     if (RESIDENT) {
 #pragma unroll
-      for (int j = 0; j < kResident; ++j) {
-        const uint32_t *qw = &qr[j].x, *kw = &kr[j].x;
+      for (int j = 0; j < QR; ++j) {
+        const int c = 32 * j + lane;
+        qr[j] = make_uint4(0, 0, 0, 0);
+        if (c < qch) qr[j] = *reinterpret_cast<const uint4*>(qrow + 8 * c);
+      }
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          aq.add_sq(bf16_lo(qw[k]));
-          aq.add_sq(bf16_hi(qw[k]));
-          ak.add_sq(bf16_lo(kw[k]));
-          ak.add_sq(bf16_hi(kw[k]));
-        }
+      for (int j = 0; j < KR; ++j) {
+        const int c = 32 * j + lane;
+        kr[j] = make_uint4(0, 0, 0, 0);
+        if (c < kch) kr[j] = *reinterpret_cast<const uint4*>(krow + 8 * c);
+      }
+#pragma unroll
+      for (int j = 0; j < QR; ++j) {
+        const uint32_t* qw = &qr[j].x;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) aq.add_sq(qw[k]);
+      }
+#pragma unroll
+      for (int j = 0; j < KR; ++j) {
+        const uint32_t* kw = &kr[j].x;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) ak.add_sq(kw[k]);
       }
     } else {
       for (int c = lane; c < qch; c += 32) {
         const uint4 v = *reinterpret_cast<const uint4*>(qrow + 8 * c);
         const uint32_t* w = &v.x;
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          aq.add_sq(bf16_lo(w[k]));
-          aq.add_sq(bf16_hi(w[k]));
-        }
+        for (int k = 0; k < 4; ++k) aq.add_sq(w[k]);
       }
       for (int c = lane; c < kch; c += 32) {
         const uint4 v = *reinterpret_cast<const uint4*>(krow + 8 * c);
         const uint32_t* w = &v.x;
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          ak.add_sq(bf16_lo(w[k]));
-          ak.add_sq(bf16_hi(w[k]));
-        }
+        for (int k = 0; k < 4; ++k) ak.add_sq(w[k]);
       }
     }
     df Sq = aq.value(), Sk = ak.value();
@@ -111,9 +109,10 @@ __global__ void __launch_bounds__(kWarps * 32) rmsnorm_mx_kernel(const MxParams 
       Sq = df_add(Sq, shfl_xor_df(Sq, s));
       Sk = df_add(Sk, shfl_xor_df(Sk, s));
     }
-    const float rq = rms_factor(mean_from_sum(Sq, (float)p.Nq, 1.0f / (float)p.Nq, q_pow2), p.eps);
-    const float rk =
-        kch ? rms_factor(mean_from_sum(Sk, (float)p.Nkv, 1.0f / (float)p.Nkv, k_pow2), p.eps) : 0.0f;
+    const f2_t rq =
+        splat2(rms_factor(mean_from_sum(Sq, (float)p.Nq, 1.0f / (float)p.Nq, q_pow2), p.eps));
+    const f2_t rk = splat2(
+        kch ? rms_factor(mean_from_sum(Sk, (float)p.Nkv, 1.0f / (float)p.Nkv, k_pow2), p.eps) : 0.0f);
 
     uint8_t* qo = p.q_out + m * p.q_out_stride;
     uint8_t* so = p.q_scale + m * p.q_scale_stride;
@@ -157,10 +156,10 @@ __global__ void __launch_bounds__(kWarps * 32) rmsnorm_mx_kernel(const MxParams 
     };
     if (RESIDENT) {
 #pragma unroll
-      for (int j = 0; j < kResident; ++j)
+      for (int j = 0; j < QR; ++j)
         if (j < qsteps) q_step(j, qr[j]);
 #pragma unroll
-      for (int j = 0; j < kResident; ++j)
+      for (int j = 0; j < KR; ++j)
         if (j < ksteps) kv_step(j, kr[j]);
     } else {
       for (int j = 0; j < qsteps; ++j) {
@@ -179,11 +178,9 @@ __global__ void __launch_bounds__(kWarps * 32) rmsnorm_mx_kernel(const MxParams 
   }
 }
 
-}  // namespace
-
-cudaError_t launch_mx(const MxParams& p, cudaStream_t stream) {
-  const bool resident = p.Nq <= 256 * kResident && p.Nkv <= 256 * kResident;
-  const void* kern = resident ? (const void*)rmsnorm_mx_kernel<true> : (const void*)rmsnorm_mx_kernel<false>;
+template <int QS, int KS>
+cudaError_t launch_variant(const MxParams& p, cudaStream_t stream) {
+  auto kern = rmsnorm_mx_kernel<QS, KS>;
   int per_sm = 0;
   cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kWarps * 32, 0);
   if (e != cudaSuccess) return e;
@@ -191,11 +188,25 @@ cudaError_t launch_mx(const MxParams& p, cudaStream_t stream) {
   const int64_t want = (int64_t)sm_count() * per_sm;
   const int64_t need = (p.M + kWarps - 1) / kWarps;
   const int grid = (int)(need < want ? need : want);
-  if (resident)
-    rmsnorm_mx_kernel<true><<<grid, kWarps * 32, 0, stream>>>(p);
-  else
-    rmsnorm_mx_kernel<false><<<grid, kWarps * 32, 0, stream>>>(p);
+  kern<<<grid, kWarps * 32, 0, stream>>>(p);
   return cudaGetLastError();
+}
+
+}  // namespace
+
+// Variant: the smallest register-resident (q steps, kv steps) pair that holds
+// the rows, else the two-pass kernel.
+cudaError_t launch_mx(const MxParams& p, cudaStream_t stream) {
+  const int qs = (p.Nq / 8 + 31) / 32, ks = (p.Nkv / 8 + 31) / 32;
+  if (ks <= 2) {
+    if (qs <= 2) return launch_variant<2, 2>(p, stream);
+    if (qs <= 4) return launch_variant<4, 2>(p, stream);
+    if (qs <= 6) return launch_variant<6, 2>(p, stream);
+    if (qs <= 8) return launch_variant<8, 2>(p, stream);
+  } else if (ks <= 8 && qs <= 8) {
+    return launch_variant<8, 8>(p, stream);
+  }
+  return launch_variant<0, 0>(p, stream);
 }
 
 }  // namespace fp8n
