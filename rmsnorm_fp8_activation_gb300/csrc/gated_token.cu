@@ -72,8 +72,51 @@ __device__ __forceinline__ uint32_t gated_pair(uint32_t xw, uint32_t ga, uint32_
 // Running max of |y| over bf16 pairs (NaN-propagating); acc stays >= 0.
 __device__ __forceinline__ uint32_t amax_step(uint32_t acc, uint32_t y) {
   uint32_t d;
-  asm("max.NaN.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(acc), "r"(y & 0x7FFF7FFFu));
+  asm("{\n .reg .b32 t;\n abs.bf16x2 t, %2;\n max.NaN.bf16x2 %0, %1, t;\n}\n"
+      : "=r"(d) : "r"(acc), "r"(y));
   return d;
+}
+
+// Gate-activation table in shared memory: entry e (0 <= e < 8192) holds
+// bf16(act(g)) for the bf16 gate with sign e >> 12 and magnitude bits
+// kLutBase + (e & 0xFFF), i.e. every gate with 2^-15 <= |g| < 2^17.  Each CTA
+// fills it once with act_bf16_pair (exact), so a lookup is the same value.
+constexpr uint32_t kLutBase = 0x3800u;  // 2^-15
+constexpr int kLutEntries = 8192;
+constexpr int kLutBytes = 2 * kLutEntries;
+
+template <int ACT>
+__device__ __forceinline__ void lut_fill(uint32_t* lut32, int tid, int nthreads) {
+  for (int w = tid; w < kLutEntries / 2; w += nthreads) {
+    const uint32_t e0 = 2u * (uint32_t)w, e1 = e0 + 1u;
+    const uint32_t g0 = ((e0 >> 12) << 15) | (kLutBase + (e0 & 0xFFFu));
+    const uint32_t g1 = ((e1 >> 12) << 15) | (kLutBase + (e1 & 0xFFFu));
+    lut32[w] = act_bf16_pair(g0 | (g1 << 16), ACT);
+  }
+}
+
+// bf16(act()) of a chunk of four gate pairs through the table.  With
+// d = |g| - base per half, both halves of every pair are in range when no
+// d has a bit in 0xF000 (a magnitude below the base borrows into those bits);
+// then 2d | (sign bits moved to bit 13) is the pair of byte offsets.  A chunk
+// with any lane out of range takes the arithmetic path for all its pairs.
+template <int ACT>
+__device__ __forceinline__ void lut_chunk(const uint8_t* lut, const uint32_t g[4], uint32_t ga[4]) {
+  uint32_t d[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) d[k] = (g[k] & 0x7FFF7FFFu) - (kLutBase | (kLutBase << 16));
+  if ((d[0] | d[1] | d[2] | d[3]) & 0xF000F000u) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) ga[k] = act_bf16_pair(g[k], ACT);
+    return;
+  }
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const uint32_t off = (d[k] * 2u) | ((g[k] >> 2) & 0x20002000u);
+    const uint32_t v0 = *reinterpret_cast<const uint16_t*>(lut + (off & 0xFFFFu));
+    const uint32_t v1 = *reinterpret_cast<const uint16_t*>(lut + (off >> 16));
+    ga[k] = __byte_perm(v0, v1, 0x5410);
+  }
 }
 
 // Token quantiser: code = e4m3(RN32(y / scale)), from the correctly rounded
@@ -95,7 +138,7 @@ struct TokenQuant {
   template <bool TINY>
   __device__ __forceinline__ uint32_t pair(uint32_t y) const {
     if (zero) return f2_to_e4m3x2(bf2_to_f2(y));
-    f2_t ny = bf2_to_f2(y ^ 0x80008000u);
+    f2_t ny = neg_bf2_to_f2(y);
     if (TINY) ny = mul2(ny, splat2(0x1p64f));
     const f2_t q0 = mul2(ny, nrs2);
     const f2_t e = fma2(q0, s2, ny);
@@ -108,7 +151,7 @@ struct TokenQuant {
   }
 };
 
-template <int ACT, int CPT, int TPH>
+template <int ACT, int CPT, int TPH, bool LUT>
 __global__ void __launch_bounds__(512) gated_token_tma(const GatedParams p, int nstage) {
   extern __shared__ __align__(1024) uint8_t smem[];
   const int row = p.H * p.D;
@@ -119,8 +162,9 @@ __global__ void __launch_bounds__(512) gated_token_tma(const GatedParams p, int 
   const bool active = tid < nthr;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
   float* red = reinterpret_cast<float*>(smem + 64);
-  uint16_t* wsm = reinterpret_cast<uint16_t*>(smem + kHeader);  // weight [D]
-  uint8_t* stages = smem + kHeader + 2 * p.D;
+  uint8_t* lut = smem + kHeader;  // at a fixed offset: its base folds into the loads
+  uint16_t* wsm = reinterpret_cast<uint16_t*>(smem + kHeader + (LUT ? kLutBytes : 0));  // weight [D]
+  uint8_t* stages = smem + kHeader + (LUT ? kLutBytes : 0) + 2 * p.D;
 
   for (int i = tid; i < p.D / 8; i += blockDim.x)
     reinterpret_cast<uint4*>(wsm)[i] = reinterpret_cast<const uint4*>(p.weight)[i];
@@ -142,6 +186,10 @@ __global__ void __launch_bounds__(512) gated_token_tma(const GatedParams p, int 
       int64_t t = blockIdx.x + (int64_t)s * gridDim.x;
       if (t < p.T) issue(s, t);
     }
+  if (LUT) {  // filled while the first rows are in flight
+    lut_fill<ACT>(reinterpret_cast<uint32_t*>(lut), tid, blockDim.x);
+    __syncthreads();
+  }
 
   const int seg = tid * 8 * CPT;  // first element of the thread's segment
   const uint16_t* wseg = wsm + (seg % p.D);
@@ -155,42 +203,44 @@ __global__ void __launch_bounds__(512) gated_token_tma(const GatedParams p, int 
     const uint8_t* sx = stages + (size_t)s * stage_bytes + (size_t)seg * 2;
     const uint8_t* sg = sx + row_bytes;
 
-    uint4 xr[CPT], ga[CPT];
+    // pass 1: the head's sum of squares (x is read again in pass 2)
     kahan2 acc;
 #pragma unroll
     for (int c = 0; c < CPT; ++c) {
-      xr[c] = ga[c] = make_uint4(0, 0, 0, 0);
-      if (active) {
-        const int off = 16 * slot_of<CPT>(c, tid);
-        xr[c] = *reinterpret_cast<const uint4*>(sx + off);
-        ga[c] = *reinterpret_cast<const uint4*>(sg + off);
-      }
-      const uint32_t* xw = &xr[c].x;
+      const uint4 xv = active ? *reinterpret_cast<const uint4*>(sx + 16 * slot_of<CPT>(c, tid))
+                              : make_uint4(0, 0, 0, 0);
+      const uint32_t* xw = &xv.x;
 #pragma unroll
       for (int k = 0; k < 4; ++k) acc.add_sq(xw[k]);
-    }
-    // the gate factors do not depend on the norm: computed while the sums
-    // reduce (inactive lanes hold zero gates, which are cheap and unused)
-#pragma unroll
-    for (int c = 0; c < CPT; ++c) {
-      uint32_t* gw = &ga[c].x;
-#pragma unroll
-      for (int k = 0; k < 4; ++k) gw[k] = act_bf16_pair(gw[k], ACT);
     }
     df S = acc.value();
 #pragma unroll
     for (int m = 1; m < TPH; m <<= 1) S = df_add(S, shfl_xor_df(S, m));
     const f2_t r2 = splat2(rms_factor(__fmul_rn(__fadd_rn(S.h, S.l), inv_d), p.eps));
 
+    // pass 2: y = bf16(bf16(bf16(x r) w) act(g)), kept as bf16 pairs
     uint32_t y[CPT][4];
     uint32_t am2 = 0;
 #pragma unroll
     for (int c = 0; c < CPT; ++c) {
+      const int off = 16 * slot_of<CPT>(c, tid);
+      uint4 xv = make_uint4(0, 0, 0, 0), gv = xv;
+      if (active) {
+        xv = *reinterpret_cast<const uint4*>(sx + off);
+        gv = *reinterpret_cast<const uint4*>(sg + off);
+      }
       const uint4 wv = *reinterpret_cast<const uint4*>(wseg + 8 * slot_of<CPT>(c, tid));
-      const uint32_t *xw = &xr[c].x, *gw = &ga[c].x, *ww = &wv.x;
+      const uint32_t *xw = &xv.x, *gw = &gv.x, *ww = &wv.x;
+      uint32_t ga[4];
+      if (LUT) {
+        lut_chunk<ACT>(lut, gw, ga);
+      } else {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) ga[k] = act_bf16_pair(gw[k], ACT);
+      }
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
-        y[c][k] = gated_pair(xw[k], gw[k], ww[k], r2);
+        y[c][k] = gated_pair(xw[k], ga[k], ww[k], r2);
         am2 = amax_step(am2, y[c][k]);
       }
     }
@@ -305,16 +355,20 @@ __global__ void __launch_bounds__(256) gated_token_generic(const GatedParams p) 
   }
 }
 
-template <int ACT, int CPT, int TPH>
-cudaError_t launch_tma(const GatedParams& p, cudaStream_t stream) {
-  auto kern = gated_token_tma<ACT, CPT, TPH>;
+// Rows of 16 KB or more get one stage per CTA, so that four CTAs fit on an SM
+// and the loads of the others overlap each CTA's compute (its own next row
+// also lands while it quantises); shorter rows get two stages.  The gate
+// table is used when each CTA walks enough tokens to pay for filling it.  The
+// grid is the SM count times the CTAs that fit.
+template <int ACT, int CPT, int TPH, bool LUT>
+cudaError_t launch_tma_v(const GatedParams& p, cudaStream_t stream) {
+  auto kern = gated_token_tma<ACT, CPT, TPH, LUT>;
   const int row = p.H * p.D;
   const int nthr = row / (8 * CPT);
   const int block = (nthr + 31) / 32 * 32;
   const size_t stage_bytes = 4u * (size_t)row;
-  int nstage = (int)((96 * 1024) / stage_bytes);
-  nstage = nstage < 2 ? 2 : (nstage > 4 ? 4 : nstage);
-  const size_t smem = kHeader + 2 * (size_t)p.D + nstage * stage_bytes;
+  const int nstage = stage_bytes >= 32 * 1024 ? 1 : 2;
+  const size_t smem = kHeader + 2 * (size_t)p.D + (LUT ? kLutBytes : 0) + nstage * stage_bytes;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   int per_sm = 0;
@@ -325,6 +379,14 @@ cudaError_t launch_tma(const GatedParams& p, cudaStream_t stream) {
   const int grid = (int)(p.T < want ? p.T : want);
   kern<<<grid, block, smem, stream>>>(p, nstage);
   return cudaGetLastError();
+}
+
+template <int ACT, int CPT, int TPH>
+cudaError_t launch_tma(const GatedParams& p, cudaStream_t stream) {
+  // the table costs about as much as 8192 / (H*D) tokens of activations per CTA
+  const int64_t per_cta = p.T / ((int64_t)sm_count() * 4);
+  if (per_cta * p.H * p.D >= 8 * kLutEntries) return launch_tma_v<ACT, CPT, TPH, true>(p, stream);
+  return launch_tma_v<ACT, CPT, TPH, false>(p, stream);
 }
 
 template <int ACT>
