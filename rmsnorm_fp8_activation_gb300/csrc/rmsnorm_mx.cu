@@ -178,6 +178,194 @@ __global__ void __launch_bounds__(kWarps * 32, (QS + KS >= 8) ? 2 : 3) rmsnorm_m
   }
 }
 
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
+                                         uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
+// Largest magnitude of four bf16 pairs as bf16 bits, over the four lanes of an
+// MX block (lanes 4b..4b+3).  Magnitude bits order like the values, with
+// infinity above every finite value and NaN above infinity.
+__device__ __forceinline__ uint32_t block_amax_bits(const uint32_t y[4]) {
+  uint32_t m01, m23, m;
+  asm("max.u16x2 %0, %1, %2;" : "=r"(m01) : "r"(y[0] & 0x7FFF7FFFu), "r"(y[1] & 0x7FFF7FFFu));
+  asm("max.u16x2 %0, %1, %2;" : "=r"(m23) : "r"(y[2] & 0x7FFF7FFFu), "r"(y[3] & 0x7FFF7FFFu));
+  asm("max.u16x2 %0, %1, %2;" : "=r"(m) : "r"(m01), "r"(m23));
+  asm("max.u16x2 %0, %1, %2;" : "=r"(m) : "r"(m), "r"(__shfl_xor_sync(0xFFFFFFFFu, m, 1)));
+  asm("max.u16x2 %0, %1, %2;" : "=r"(m) : "r"(m), "r"(__shfl_xor_sync(0xFFFFFFFFu, m, 2)));
+  return max(m & 0xFFFFu, m >> 16);
+}
+
+// E8M0 code of a block from its amax bits A: floor(log2 A) is the exponent
+// field minus 127 for a normal A, so code = e + 127 = field - 8, clamped at 0
+// (which also covers zero and subnormal blocks); 0xFF for NaN or infinity.
+__device__ __forceinline__ uint32_t mx_code(uint32_t A) {
+  const uint32_t ef = A >> 7;
+  return ef == 0xFFu ? 0xFFu : (ef > 8u ? ef - 8u : 0u);
+}
+
+// Staged variant for rows that fit two per-warp slots: each warp owns two
+// shared-memory slots (q row then kv row) filled by cp.async.bulk on its own
+// mbarriers, and starts the copy of its next-but-one row as soon as a slot is
+// consumed, so row loads overlap the arithmetic of the row before.  Lane l
+// reads chunks l, l+32, ... of the slot (consecutive 16-byte words: no bank
+// conflicts) in both passes.
+constexpr int kSlots = 2;
+constexpr int kStagedMaxWarps = 16;
+// mbarriers of every warp (8 bytes per slot), ahead of the row slots
+constexpr int kStagedHeader = kStagedMaxWarps * kSlots * 8;
+static_assert(kStagedHeader % 128 == 0, "row slots start 128-byte aligned");
+
+__global__ void __launch_bounds__(kStagedMaxWarps * 32) rmsnorm_mx_tma(const MxParams p) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, wpb = blockDim.x >> 5;
+  const int64_t gwarp = (int64_t)blockIdx.x * wpb + warp;
+  const int64_t nwarps = (int64_t)gridDim.x * wpb;
+  const int qch = p.Nq / 8, kch = p.Nkv / 8;
+  const uint32_t qbytes = 2u * (uint32_t)p.Nq, kbytes = 2u * (uint32_t)p.Nkv;
+  const uint32_t slot_bytes = qbytes + kbytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem) + warp * kSlots;
+  uint8_t* slots = smem + kStagedHeader + (size_t)warp * kSlots * slot_bytes;
+  const bool q_pow2 = (p.Nq & (p.Nq - 1)) == 0, k_pow2 = (p.Nkv & (p.Nkv - 1)) == 0;
+
+  if (lane == 0) {
+    for (int s = 0; s < kSlots; ++s) mbar_init(smem_u32(&bars[s]), 1);
+    asm volatile("fence.mbarrier_init.release.cluster;\n fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  __syncwarp();
+  auto issue = [&](int s, int64_t m) {
+    const uint32_t bar = smem_u32(&bars[s]);
+    const uint32_t dst = smem_u32(slots + (size_t)s * slot_bytes);
+    mbar_expect_tx(bar, slot_bytes);
+    bulk_g2s(dst, p.q + m * p.q_stride, qbytes, bar);
+    if (kbytes) bulk_g2s(dst + qbytes, p.kv + m * p.kv_stride, kbytes, bar);
+  };
+  if (lane == 0)
+    for (int s = 0; s < kSlots; ++s) {
+      const int64_t m = gwarp + s * nwarps;
+      if (m < p.M) issue(s, m);
+    }
+
+  int it = 0;
+  bool timeout = false;
+  for (int64_t m = gwarp; m < p.M; m += nwarps, ++it) {
+    const int s = it % kSlots;
+    if (!mbar_wait(smem_u32(&bars[s]), (uint32_t)(it / kSlots) & 1u, kWaitLimit)) timeout = true;
+    if (__any_sync(0xFFFFFFFFu, timeout)) break;
+    const uint4* sq = reinterpret_cast<const uint4*>(slots + (size_t)s * slot_bytes);
+    const uint4* sk = reinterpret_cast<const uint4*>(slots + (size_t)s * slot_bytes + qbytes);
+    kahan2 aq, ak;
+    for (int c = lane; c < qch; c += 32) {
+      const uint4 v = sq[c];
+      const uint32_t* w = &v.x;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) aq.add_sq(w[k]);
+    }
+    for (int c = lane; c < kch; c += 32) {
+      const uint4 v = sk[c];
+      const uint32_t* w = &v.x;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) ak.add_sq(w[k]);
+    }
+    df Sq = aq.value(), Sk = ak.value();
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) {
+      Sq = df_add(Sq, shfl_xor_df(Sq, o));
+      Sk = df_add(Sk, shfl_xor_df(Sk, o));
+    }
+    const f2_t rq =
+        splat2(rms_factor(mean_from_sum(Sq, (float)p.Nq, 1.0f / (float)p.Nq, q_pow2), p.eps));
+    const f2_t rk = splat2(
+        kch ? rms_factor(mean_from_sum(Sk, (float)p.Nkv, 1.0f / (float)p.Nkv, k_pow2), p.eps) : 0.0f);
+    uint8_t* qo = p.q_out + m * p.q_out_stride;
+    uint8_t* so = p.q_scale + m * p.q_scale_stride;
+    uint16_t* ko = p.kv_out + m * p.kv_out_stride;
+    const int qsteps = (qch + 31) / 32;
+    for (int j = 0; j < qsteps; ++j) {  // warp-uniform: every lane takes part in the shuffles
+      const int c = 32 * j + lane;
+      uint4 xv = make_uint4(0, 0, 0, 0), wv = xv;
+      if (c < qch) {
+        xv = sq[c];
+        wv = *reinterpret_cast<const uint4*>(p.q_weight + 8 * c);
+      }
+      uint32_t y[4];
+      norm_chunk(xv, wv, rq, y);
+      const uint32_t code = mx_code(block_amax_bits(y));
+      if (c < qch) {
+        if ((lane & 3) == 0) so[c >> 2] = (uint8_t)code;
+        uint2 o;
+        if (code == 0xFFu) {
+          o = make_uint2(0x7F7F7F7Fu, 0x7F7F7F7Fu);
+        } else {
+          const f2_t sc = splat2(pow2i(127 - (int)code));  // 2^-e, exact scaling
+          uint32_t b[4];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) b[k] = f2_to_e4m3x2(mul2(bf2_to_f2(y[k]), sc));
+          o = make_uint2(b[0] | (b[1] << 16), b[2] | (b[3] << 16));
+        }
+        *reinterpret_cast<uint2*>(qo + 8 * c) = o;
+      }
+    }
+    for (int c = lane; c < kch; c += 32) {
+      const uint4 wv = *reinterpret_cast<const uint4*>(p.kv_weight + 8 * c);
+      uint4 o;
+      norm_chunk(sk[c], wv, rk, &o.x);
+      *reinterpret_cast<uint4*>(ko + 8 * c) = o;
+    }
+    __syncwarp();  // every lane is done with slot s
+    if (lane == 0) {
+      const int64_t mn = m + kSlots * nwarps;
+      if (mn < p.M) issue(s, mn);
+    }
+  }
+  if (timeout && lane == 0) {
+    if (p.status) atomicOr(p.status, kStatusTimeout);
+    for (int i = it; i < it + kSlots; ++i) {
+      const int64_t mi = gwarp + (int64_t)i * nwarps;
+      if (mi < p.M) mbar_wait(smem_u32(&bars[i % kSlots]), (uint32_t)(i / kSlots) & 1u, kWaitLimit);
+    }
+  }
+}
+
+// Warps per CTA: the count (up to 16) whose CTAs pack the most warps into an
+// SM's shared memory (two row slots per warp); a row per warp-slot pair keeps
+// the slowest warp at as few rows as the SM count allows.
+cudaError_t launch_staged(const MxParams& p, cudaStream_t stream) {
+  const size_t per_warp = (size_t)kSlots * 2 * (size_t)(p.Nq + p.Nkv);
+  const size_t budget = 227 * 1024;
+  int best_w = 8, best_total = 0;
+  for (int w = 4; w <= kStagedMaxWarps; ++w) {
+    const size_t cta = kStagedHeader + w * per_warp + 1024;  // + the per-CTA reservation
+    const int ctas = (int)(budget / cta);
+    const int total = ctas * w > 64 ? 64 / w * w : ctas * w;  // 64 warps per SM at most
+    if (total > best_total) { best_total = total; best_w = w; }
+  }
+  const size_t smem = kStagedHeader + (size_t)best_w * per_warp;
+  cudaError_t e =
+      cudaFuncSetAttribute(rmsnorm_mx_tma, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  int per_sm = 0;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, rmsnorm_mx_tma, best_w * 32, smem);
+  if (e != cudaSuccess) return e;
+  if (per_sm < 1) per_sm = 1;
+  const int64_t want = (int64_t)sm_count() * per_sm;
+  const int64_t need = (p.M + best_w - 1) / best_w;
+  const int grid = (int)(need < want ? need : want);
+  rmsnorm_mx_tma<<<grid, best_w * 32, smem, stream>>>(p);
+  return cudaGetLastError();
+}
+
 template <int QS, int KS>
 cudaError_t launch_variant(const MxParams& p, cudaStream_t stream) {
   auto kern = rmsnorm_mx_kernel<QS, KS>;
@@ -194,9 +382,12 @@ cudaError_t launch_variant(const MxParams& p, cudaStream_t stream) {
 
 }  // namespace
 
-// Variant: the smallest register-resident (q steps, kv steps) pair that holds
-// the rows, else the two-pass kernel.
+// Variant: the staged kernel for rows up to 3072 elements, else the smallest
+// register-resident (q steps, kv steps) pair that holds the rows, else the
+// two-pass kernel.
 cudaError_t launch_mx(const MxParams& p, cudaStream_t stream) {
+  // rows of up to 3072 elements (q + kv): the staged kernel, 96 KB per CTA at most
+  if (p.Nq + p.Nkv <= 3072) return launch_staged(p, stream);
   const int qs = (p.Nq / 8 + 31) / 32, ks = (p.Nkv / 8 + 31) / 32;
   if (ks <= 2) {
     if (qs <= 2) return launch_variant<2, 2>(p, stream);
