@@ -76,6 +76,20 @@ def load_library(path: str) -> ctypes.CDLL:
     L.oracle_rmsnorm_quant_mx.restype = None
     L.oracle_static_head_quant.argtypes = [P, i64, i64, i64, i32, i32, P, P]
     L.oracle_static_head_quant.restype = None
+    L.oracle_quant_row.argtypes = [P, i64, P, P]
+    L.oracle_quant_row.restype = None
+    L.oracle_gated_rmsnorm_row.argtypes = [P, P, P, i32, i32, f32, ctypes.c_int, P]
+    L.oracle_gated_rmsnorm_row.restype = None
+    L.oracle_gated_quant_row.argtypes = [P, P, i64, ctypes.c_int, P, P, P]
+    L.oracle_gated_quant_row.restype = None
+    L.oracle_rmsnorm_row.argtypes = [P, P, i32, f32, P]
+    L.oracle_rmsnorm_row.restype = None
+    L.oracle_quant_mx_row.argtypes = [P, i32, P, P]
+    L.oracle_quant_mx_row.restype = None
+    L.oracle_head_amax.argtypes = [P, i64, i64, i64, i32, i32, P]
+    L.oracle_head_amax.restype = None
+    L.oracle_dynamic_head_quant.argtypes = [P, i64, i64, i64, i32, i32, P, P]
+    L.oracle_dynamic_head_quant.restype = None
     return L
 
 
@@ -221,3 +235,86 @@ def static_head_quant(x, descale):
     out = np.zeros((T, H, Dh), dtype=np.uint8)
     lib().oracle_static_head_quant(_ptr(x), H * Dh, Dh, T, H, Dh, _ptr(descale), _ptr(out))
     return out
+
+
+# ---- the steps of (A) and (B) on their own, and the dynamic per-head quant ----
+
+def quant_token(y):
+    """Per-token FP8 of bf16 rows y [T, N]: (codes uint8 [T, N], scale float32 [T])."""
+    y = _c(y, np.uint16)
+    T, N = y.shape
+    out = np.zeros((T, N), dtype=np.uint8)
+    scale = np.zeros((T,), dtype=np.float32)
+    for t in range(T):
+        lib().oracle_quant_row(_ptr(y[t]), N, _ptr(out[t]), scale[t:].ctypes.data)
+    return out, scale
+
+
+def gated_rmsnorm_bf16(x, gate, weight, eps: float, act: int):
+    """(A) without the quantisation: y bf16 bits [T, H*D]."""
+    x = _c(x, np.uint16)
+    gate = _c(gate, np.uint16)
+    weight = _c(weight, np.uint16)
+    T, H, D = x.shape
+    y = np.zeros((T, H * D), dtype=np.uint16)
+    for t in range(T):
+        lib().oracle_gated_rmsnorm_row(_ptr(x[t]), _ptr(gate[t]), _ptr(weight), H, D, float(eps),
+                                       int(act), _ptr(y[t]))
+    return y
+
+
+def gated_quant_token(x, gate, act: int):
+    """y = bf16(x * bf16(act(gate))) per element of [T, N], then per-token FP8.
+    Returns (y bf16 bits, codes, scale)."""
+    x = _c(x, np.uint16)
+    gate = _c(gate, np.uint16)
+    T, N = x.shape
+    y = np.zeros((T, N), dtype=np.uint16)
+    out = np.zeros((T, N), dtype=np.uint8)
+    scale = np.zeros((T,), dtype=np.float32)
+    for t in range(T):
+        lib().oracle_gated_quant_row(_ptr(x[t]), _ptr(gate[t]), N, int(act), _ptr(y[t]),
+                                     _ptr(out[t]), scale[t:].ctypes.data)
+    return y, out, scale
+
+
+def rmsnorm_bf16(x, weight, eps: float):
+    """Row RMSNorm of bf16 rows x [M, N] with weight [N]: bf16 bits [M, N]."""
+    x = _c(x, np.uint16)
+    weight = _c(weight, np.uint16)
+    M, N = x.shape
+    y = np.zeros((M, N), dtype=np.uint16)
+    for m in range(M):
+        lib().oracle_rmsnorm_row(_ptr(x[m]), _ptr(weight), N, float(eps), _ptr(y[m]))
+    return y
+
+
+def quant_mx(yq):
+    """MX quantisation of bf16 rows yq [M, N] (N % 32 == 0): (codes [M, N], E8M0 [M, N/32])."""
+    yq = _c(yq, np.uint16)
+    M, N = yq.shape
+    assert N % 32 == 0
+    codes = np.zeros((M, N), dtype=np.uint8)
+    scales = np.zeros((M, N // 32), dtype=np.uint8)
+    for m in range(M):
+        lib().oracle_quant_mx_row(_ptr(yq[m]), N, _ptr(codes[m]), _ptr(scales[m]))
+    return codes, scales
+
+
+def head_amax(x, amax=None):
+    """Running per-head max of |x| for x [T, H, Dh]; returns the updated float32 [H]."""
+    x = _c(x, np.uint16)
+    T, H, Dh = x.shape
+    a = np.zeros((H,), dtype=np.float32) if amax is None else np.array(amax, dtype=np.float32)
+    lib().oracle_head_amax(_ptr(x), H * Dh, Dh, T, H, Dh, _ptr(a))
+    return a
+
+
+def dynamic_head_quant(x):
+    """Per-head descales from the tensor's own maxima, then codes: (descale [H], codes)."""
+    x = _c(x, np.uint16)
+    T, H, Dh = x.shape
+    d = np.zeros((H,), dtype=np.float32)
+    out = np.zeros((T, H, Dh), dtype=np.uint8)
+    lib().oracle_dynamic_head_quant(_ptr(x), H * Dh, Dh, T, H, Dh, _ptr(d), _ptr(out))
+    return d, out

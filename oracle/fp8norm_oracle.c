@@ -238,10 +238,33 @@ static uint16_t norm_times_weight(uint16_t xb, float r, uint16_t wb) {
  * scale = RN32(amax / 448) (448 = largest finite E4M3), code =
  * e4m3(RN32(y / scale)).  A token whose amax is zero gets scale 0 and codes
  * that are zeros carrying the sign of y (no epsilon floor on the scale). */
-void oracle_gated_rmsnorm_quant_one(const uint16_t* x_tok, const uint16_t* gate_tok,
-                                    const uint16_t* weight, int32_t H, int32_t D,
-                                    float eps, int act, uint16_t* y_tok,
-                                    uint8_t* out_tok, float* scale_tok) {
+/* Per-token quantisation of a bf16 row y[n] ([GATED] wrapper: one scale over
+ * the whole [heads*h] row).  Also the standalone per-token quant applied to an
+ * already-normalised row in the same page's decode path. */
+void oracle_quant_row(const uint16_t* y, int64_t n, uint8_t* out, float* scale_out) {
+  double amax = 0.0;
+  int any_nan = 0;
+  for (int64_t i = 0; i < n; ++i) {
+    double a = fabs(oracle_bf16_to_double(y[i]));
+    if (isnan(a)) any_nan = 1;
+    else if (a > amax) amax = a;
+  }
+  float famax = any_nan ? NAN : (float)amax; /* exact: amax is a bf16 value */
+  float scale = famax / 448.0f;
+  *scale_out = scale;
+  for (int64_t i = 0; i < n; ++i) {
+    float yv = (float)oracle_bf16_to_double(y[i]);
+    if (famax == 0.0f)
+      out[i] = (y[i] & 0x8000) ? 0x80 : 0x00;
+    else
+      out[i] = oracle_e4m3_from_float(yv / scale);
+  }
+}
+
+/* y = bf16(bf16(bf16(RN32(x * r)) * w) * bf16(act(g))) for one token, heads of D. */
+void oracle_gated_rmsnorm_row(const uint16_t* x_tok, const uint16_t* gate_tok,
+                              const uint16_t* weight, int32_t H, int32_t D, float eps, int act,
+                              uint16_t* y_tok) {
   for (int32_t h = 0; h < H; ++h) {
     const uint16_t* xh = x_tok + (int64_t)h * D;
     const uint16_t* gh = gate_tok + (int64_t)h * D;
@@ -253,24 +276,14 @@ void oracle_gated_rmsnorm_quant_one(const uint16_t* x_tok, const uint16_t* gate_
           oracle_bf16_from_double(oracle_bf16_to_double(u) * oracle_bf16_to_double(g));
     }
   }
-  int64_t n = (int64_t)H * D;
-  double amax = 0.0;
-  int any_nan = 0;
-  for (int64_t i = 0; i < n; ++i) {
-    double a = fabs(oracle_bf16_to_double(y_tok[i]));
-    if (isnan(a)) any_nan = 1;
-    else if (a > amax) amax = a;
-  }
-  float famax = any_nan ? NAN : (float)amax; /* exact: amax is a bf16 value */
-  float scale = famax / 448.0f;
-  *scale_tok = scale;
-  for (int64_t i = 0; i < n; ++i) {
-    float yv = (float)oracle_bf16_to_double(y_tok[i]);
-    if (famax == 0.0f)
-      out_tok[i] = (y_tok[i] & 0x8000) ? 0x80 : 0x00;
-    else
-      out_tok[i] = oracle_e4m3_from_float(yv / scale);
-  }
+}
+
+void oracle_gated_rmsnorm_quant_one(const uint16_t* x_tok, const uint16_t* gate_tok,
+                                    const uint16_t* weight, int32_t H, int32_t D,
+                                    float eps, int act, uint16_t* y_tok,
+                                    uint8_t* out_tok, float* scale_tok) {
+  oracle_gated_rmsnorm_row(x_tok, gate_tok, weight, H, D, eps, act, y_tok);
+  oracle_quant_row(y_tok, (int64_t)H * D, out_tok, scale_tok);
 }
 
 void oracle_gated_rmsnorm_quant_token(const uint16_t* x, int64_t x_stride,
@@ -284,6 +297,18 @@ void oracle_gated_rmsnorm_quant_token(const uint16_t* x, int64_t x_stride,
     oracle_gated_rmsnorm_quant_one(x + t * x_stride, gate + t * gate_stride, weight, H, D,
                                    eps, act, y, out + t * out_stride, scale + t);
   free(y);
+}
+
+/* Gated per-token quant without the norm: y = bf16(x * bf16(act(g))), then the
+ * per-token quantisation.  The gate product in the activation dtype follows
+ * [GATED]'s helper; the sigmoid-mul + per-token FP8 epilogue of the MLA o_proj
+ * named on that page is this map with the sigmoid. */
+void oracle_gated_quant_row(const uint16_t* x, const uint16_t* gate, int64_t n, int act,
+                            uint16_t* y, uint8_t* out, float* scale) {
+  for (int64_t i = 0; i < n; ++i)
+    y[i] = oracle_bf16_from_double(oracle_bf16_to_double(x[i]) *
+                                   oracle_bf16_to_double(oracle_act_bf16(gate[i], act)));
+  oracle_quant_row(y, n, out, scale);
 }
 
 /* ===================================================================== */
@@ -307,7 +332,7 @@ uint8_t oracle_e8m0_code(uint16_t amax_bits) {
 }
 
 /* Normalised bf16 row: bf16(bf16(RN32(x * r)) * w), r from the full row. */
-static void rmsnorm_row(const uint16_t* x, const uint16_t* w, int32_t n, float eps,
+void oracle_rmsnorm_row(const uint16_t* x, const uint16_t* w, int32_t n, float eps,
                         uint16_t* y) {
   float r = oracle_rms_factor(oracle_mean_square_bf16(x, n), eps);
   for (int32_t j = 0; j < n; ++j) y[j] = norm_times_weight(x[j], r, w[j]);
@@ -326,9 +351,18 @@ void oracle_rmsnorm_quant_mx(const uint16_t* q, int64_t q_stride, const uint16_t
                              int64_t kv_out_stride) {
   uint16_t* yq = (uint16_t*)malloc((size_t)(Nq > 0 ? Nq : 1) * sizeof(uint16_t));
   for (int64_t m = 0; m < M; ++m) {
-    if (Nq > 0) rmsnorm_row(q + m * q_stride, q_weight, Nq, eps, yq);
-    if (Nkv > 0) rmsnorm_row(kv + m * kv_stride, kv_weight, Nkv, eps, kv_out + m * kv_out_stride);
-    for (int32_t b = 0; b < Nq / 32; ++b) {
+    if (Nq > 0) oracle_rmsnorm_row(q + m * q_stride, q_weight, Nq, eps, yq);
+    if (Nkv > 0) oracle_rmsnorm_row(kv + m * kv_stride, kv_weight, Nkv, eps, kv_out + m * kv_out_stride);
+    oracle_quant_mx_row(yq, Nq, q_out + m * q_out_stride, q_scale + m * q_scale_stride);
+  }
+  free(yq);
+}
+
+/* MX quantisation of one bf16 row of n (a multiple of 32) values: per block of
+ * 32, the E8M0 code of its amax and the E4M3 codes of the scaled elements. */
+void oracle_quant_mx_row(const uint16_t* yq, int32_t n, uint8_t* codes, uint8_t* scales) {
+  {
+    for (int32_t b = 0; b < n / 32; ++b) {
       const uint16_t* blk = yq + 32 * b;
       uint16_t amax_bits = 0;
       double amax = 0.0;
@@ -339,8 +373,8 @@ void oracle_rmsnorm_quant_mx(const uint16_t* q, int64_t q_stride, const uint16_t
         else if (a > amax) { amax = a; amax_bits = blk[j] & 0x7FFF; }
       }
       uint8_t code = bad ? 0xFF : oracle_e8m0_code(amax_bits);
-      q_scale[m * q_scale_stride + b] = code;
-      uint8_t* o = q_out + m * q_out_stride + 32 * b;
+      scales[b] = code;
+      uint8_t* o = codes + 32 * b;
       for (int j = 0; j < 32; ++j) {
         if (code == 0xFF) { o[j] = 0x7F; continue; }
         double scaled = ldexp(oracle_bf16_to_double(blk[j]), -((int)code - 127));
@@ -350,7 +384,6 @@ void oracle_rmsnorm_quant_mx(const uint16_t* q, int64_t q_stride, const uint16_t
       }
     }
   }
-  free(yq);
 }
 
 /* ===================================================================== */
@@ -369,5 +402,43 @@ void oracle_static_head_quant(const uint16_t* x, int64_t tok_stride, int64_t hea
       for (int32_t d = 0; d < Dh; ++d) {
         float xv = (float)oracle_bf16_to_double(x[t * tok_stride + h * head_stride + d]);
         out[(t * H + h) * Dh + d] = oracle_e4m3_from_float(xv / descale[h]);
+      }
+}
+
+/* Running per-head maximum of |x| over all tokens and d ([STATIC]: the layer
+ * collects Q/K/V maxima in calibration mode; the dynamic path these static
+ * scales replace reduces the same maxima on every step).  amax[h] is updated
+ * in place: amax[h] = max(amax[h], max |x[:, h, :]|); NaN propagates. */
+void oracle_head_amax(const uint16_t* x, int64_t tok_stride, int64_t head_stride, int64_t T,
+                      int32_t H, int32_t Dh, float* amax) {
+  for (int32_t h = 0; h < H; ++h) {
+    double m = (double)amax[h];
+    int nan = isnan(m);
+    for (int64_t t = 0; t < T; ++t)
+      for (int32_t d = 0; d < Dh; ++d) {
+        double a = fabs(oracle_bf16_to_double(x[t * tok_stride + h * head_stride + d]));
+        if (isnan(a)) nan = 1;
+        else if (a > m) m = a;
+      }
+    amax[h] = nan ? NAN : (float)m;
+  }
+}
+
+/* Dynamic per-head quant: descale[h] = RN32(amax[h] / 448) from this tensor's
+ * own maxima, then the static map with those descales; a head whose amax is 0
+ * gets descale 0 and signed zero codes (the zero-token rule of the per-token
+ * quantiser, applied per head). */
+void oracle_dynamic_head_quant(const uint16_t* x, int64_t tok_stride, int64_t head_stride,
+                               int64_t T, int32_t H, int32_t Dh, float* descale, uint8_t* out) {
+  for (int32_t h = 0; h < H; ++h) descale[h] = 0.0f;
+  oracle_head_amax(x, tok_stride, head_stride, T, H, Dh, descale);
+  for (int32_t h = 0; h < H; ++h) descale[h] = descale[h] / 448.0f;
+  for (int64_t t = 0; t < T; ++t)
+    for (int32_t h = 0; h < H; ++h)
+      for (int32_t d = 0; d < Dh; ++d) {
+        uint16_t b = x[t * tok_stride + h * head_stride + d];
+        float xv = (float)oracle_bf16_to_double(b);
+        out[(t * H + h) * Dh + d] = descale[h] == 0.0f ? ((b & 0x8000) ? 0x80 : 0x00)
+                                                       : oracle_e4m3_from_float(xv / descale[h]);
       }
 }

@@ -85,6 +85,19 @@ void oracle_gated_rmsnorm_quant_one(const uint16_t* x_tok, const uint16_t* gate_
                                     float eps, int act, uint16_t* y_tok,
                                     uint8_t* out_tok, float* scale_tok);
 
+/* ---- the steps of (A), each on its own --------------------------------- */
+/* Per-token quantisation of one bf16 row y[n]: scale = RN32(max|y| / 448),
+ * codes e4m3(RN32(y / scale)); a zero row gets scale 0 and signed zeros. */
+void oracle_quant_row(const uint16_t* y, int64_t n, uint8_t* out, float* scale);
+/* (A) without the quantisation: y [H*D] bf16 for one token. */
+void oracle_gated_rmsnorm_row(const uint16_t* x_tok, const uint16_t* gate_tok,
+                              const uint16_t* weight, int32_t H, int32_t D, float eps, int act,
+                              uint16_t* y_tok);
+/* Gate product without the norm, then the per-token quantisation:
+ * y = bf16(x * bf16(act(gate))) over n values. */
+void oracle_gated_quant_row(const uint16_t* x, const uint16_t* gate, int64_t n, int act,
+                            uint16_t* y, uint8_t* out, float* scale);
+
 /* ---- operation (B): fused q/kv RMSNorm, q -> MXFP8, kv -> bf16 ---------- */
 /* q: [M, Nq] bf16 (row stride q_stride), kv: [M, Nkv] bf16 (kv_stride);
  * Nq % 32 == 0.  q_out: e4m3 [M, Nq]; q_scale: E8M0 [M, Nq/32] row-major;
@@ -96,6 +109,11 @@ void oracle_rmsnorm_quant_mx(const uint16_t* q, int64_t q_stride, const uint16_t
                              int64_t q_scale_stride, uint16_t* kv_out,
                              int64_t kv_out_stride);
 
+/* The steps of (B): one normalised bf16 row, and the MX quantisation of a
+ * bf16 row (n a multiple of 32; codes [n], E8M0 scales [n/32]). */
+void oracle_rmsnorm_row(const uint16_t* x, const uint16_t* w, int32_t n, float eps, uint16_t* y);
+void oracle_quant_mx_row(const uint16_t* yq, int32_t n, uint8_t* codes, uint8_t* scales);
+
 /* E8M0 code of a block whose largest magnitude is the bf16 value `amax`. */
 uint8_t oracle_e8m0_code(uint16_t amax_bits);
 
@@ -105,6 +123,15 @@ uint8_t oracle_e8m0_code(uint16_t amax_bits);
 void oracle_static_head_quant(const uint16_t* x, int64_t tok_stride, int64_t head_stride,
                               int64_t T, int32_t H, int32_t Dh, const float* descale,
                               uint8_t* out);
+
+/* ---- dynamic per-head quant (what the static scales replace) ----------- */
+/* amax[h] = max(amax[h], max over t, d of |x[t, h, d]|), NaN-propagating. */
+void oracle_head_amax(const uint16_t* x, int64_t tok_stride, int64_t head_stride, int64_t T,
+                      int32_t H, int32_t Dh, float* amax);
+/* descale[h] = RN32(amax_h / 448) of this tensor, then codes as in (C); a zero
+ * head gets descale 0 and signed zero codes. */
+void oracle_dynamic_head_quant(const uint16_t* x, int64_t tok_stride, int64_t head_stride,
+                               int64_t T, int32_t H, int32_t Dh, float* descale, uint8_t* out);
 
 #ifdef __cplusplus
 }

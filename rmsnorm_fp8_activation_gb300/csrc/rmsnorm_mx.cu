@@ -28,10 +28,18 @@ __device__ __forceinline__ float fmax_nan(float a, float b) {
 }
 
 // bf16(bf16(RN32(x * r)) * w) for a chunk of 8 (4 pairs).
+__device__ __forceinline__ uint32_t norm_pair(uint32_t x, uint32_t w, f2_t r2) {
+  return mul_bf16x2(f2_to_bf2(mul2(bf2_to_f2(x), r2)), w);
+}
 __device__ __forceinline__ void norm_chunk(const uint4& xv, const uint4& wv, f2_t r2, uint32_t y[4]) {
-  const uint32_t *xw = &xv.x, *ww = &wv.x;
-#pragma unroll
-  for (int k = 0; k < 4; ++k) y[k] = mul_bf16x2(f2_to_bf2(mul2(bf2_to_f2(xw[k]), r2)), ww[k]);
+  y[0] = norm_pair(xv.x, wv.x, r2);
+  y[1] = norm_pair(xv.y, wv.y, r2);
+  y[2] = norm_pair(xv.z, wv.z, r2);
+  y[3] = norm_pair(xv.w, wv.w, r2);
+}
+__device__ __forceinline__ uint4 norm_chunk4(const uint4& xv, const uint4& wv, f2_t r2) {
+  return make_uint4(norm_pair(xv.x, wv.x, r2), norm_pair(xv.y, wv.y, r2), norm_pair(xv.z, wv.z, r2),
+                    norm_pair(xv.w, wv.w, r2));
 }
 
 // E8M0 exponent e (scale 2^e) of a block whose amax has bf16 bits A (>= 0):
@@ -150,9 +158,7 @@ __global__ void __launch_bounds__(kWarps * 32, (QS + KS >= 8) ? 2 : 3) rmsnorm_m
       const int c = 32 * j + lane;
       if (c >= kch) return;
       const uint4 wv = *reinterpret_cast<const uint4*>(p.kv_weight + 8 * c);
-      uint4 o;
-      norm_chunk(xv, wv, rk, &o.x);
-      *reinterpret_cast<uint4*>(ko + 8 * c) = o;
+      *reinterpret_cast<uint4*>(ko + 8 * c) = norm_chunk4(xv, wv, rk);
     };
     if (RESIDENT) {
 #pragma unroll
@@ -195,16 +201,18 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
 }
 
 // Largest magnitude of four bf16 pairs as bf16 bits, over the four lanes of an
-// MX block (lanes 4b..4b+3).  Magnitude bits order like the values, with
-// infinity above every finite value and NaN above infinity.
+// MX block (lanes 4b..4b+3); NaN-propagating.
+__device__ __forceinline__ uint32_t absmax2(uint32_t acc, uint32_t y) {  // acc >= 0
+  uint32_t d;
+  asm("{\n .reg .b32 t;\n abs.bf16x2 t, %2;\n max.NaN.bf16x2 %0, %1, t;\n}\n"
+      : "=r"(d) : "r"(acc), "r"(y));
+  return d;
+}
 __device__ __forceinline__ uint32_t block_amax_bits(const uint32_t y[4]) {
-  uint32_t m01, m23, m;
-  asm("max.u16x2 %0, %1, %2;" : "=r"(m01) : "r"(y[0] & 0x7FFF7FFFu), "r"(y[1] & 0x7FFF7FFFu));
-  asm("max.u16x2 %0, %1, %2;" : "=r"(m23) : "r"(y[2] & 0x7FFF7FFFu), "r"(y[3] & 0x7FFF7FFFu));
-  asm("max.u16x2 %0, %1, %2;" : "=r"(m) : "r"(m01), "r"(m23));
-  asm("max.u16x2 %0, %1, %2;" : "=r"(m) : "r"(m), "r"(__shfl_xor_sync(0xFFFFFFFFu, m, 1)));
-  asm("max.u16x2 %0, %1, %2;" : "=r"(m) : "r"(m), "r"(__shfl_xor_sync(0xFFFFFFFFu, m, 2)));
-  return max(m & 0xFFFFu, m >> 16);
+  uint32_t m = absmax2(absmax2(absmax2(absmax2(0u, y[0]), y[1]), y[2]), y[3]);
+  m = absmax2(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
+  m = absmax2(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
+  return __float_as_uint(fmax_nan(bf16_lo(m), bf16_hi(m))) >> 16;
 }
 
 // E8M0 code of a block from its amax bits A: floor(log2 A) is the exponent
@@ -236,8 +244,14 @@ __global__ void __launch_bounds__(kStagedMaxWarps * 32) rmsnorm_mx_tma(const MxP
   const uint32_t qbytes = 2u * (uint32_t)p.Nq, kbytes = 2u * (uint32_t)p.Nkv;
   const uint32_t slot_bytes = qbytes + kbytes;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem) + warp * kSlots;
-  uint8_t* slots = smem + kStagedHeader + (size_t)warp * kSlots * slot_bytes;
+  const uint4* wq = reinterpret_cast<const uint4*>(smem + kStagedHeader);  // weights, once per CTA
+  const uint4* wk = wq + qch;
+  uint8_t* slots = smem + kStagedHeader + slot_bytes + (size_t)warp * kSlots * slot_bytes;
   const bool q_pow2 = (p.Nq & (p.Nq - 1)) == 0, k_pow2 = (p.Nkv & (p.Nkv - 1)) == 0;
+  for (int i = threadIdx.x; i < qch + kch; i += blockDim.x)
+    const_cast<uint4*>(wq)[i] = i < qch ? reinterpret_cast<const uint4*>(p.q_weight)[i]
+                                        : reinterpret_cast<const uint4*>(p.kv_weight)[i - qch];
+  __syncthreads();
 
   if (lane == 0) {
     for (int s = 0; s < kSlots; ++s) mbar_init(smem_u32(&bars[s]), 1);
@@ -297,7 +311,7 @@ __global__ void __launch_bounds__(kStagedMaxWarps * 32) rmsnorm_mx_tma(const MxP
       uint4 xv = make_uint4(0, 0, 0, 0), wv = xv;
       if (c < qch) {
         xv = sq[c];
-        wv = *reinterpret_cast<const uint4*>(p.q_weight + 8 * c);
+        wv = wq[c];
       }
       uint32_t y[4];
       norm_chunk(xv, wv, rq, y);
@@ -317,12 +331,8 @@ __global__ void __launch_bounds__(kStagedMaxWarps * 32) rmsnorm_mx_tma(const MxP
         *reinterpret_cast<uint2*>(qo + 8 * c) = o;
       }
     }
-    for (int c = lane; c < kch; c += 32) {
-      const uint4 wv = *reinterpret_cast<const uint4*>(p.kv_weight + 8 * c);
-      uint4 o;
-      norm_chunk(sk[c], wv, rk, &o.x);
-      *reinterpret_cast<uint4*>(ko + 8 * c) = o;
-    }
+    for (int c = lane; c < kch; c += 32)
+      *reinterpret_cast<uint4*>(ko + 8 * c) = norm_chunk4(sk[c], wk[c], rk);
     __syncwarp();  // every lane is done with slot s
     if (lane == 0) {
       const int64_t mn = m + kSlots * nwarps;
@@ -345,13 +355,14 @@ cudaError_t launch_staged(const MxParams& p, cudaStream_t stream) {
   const size_t per_warp = (size_t)kSlots * 2 * (size_t)(p.Nq + p.Nkv);
   const size_t budget = 227 * 1024;
   int best_w = 8, best_total = 0;
+  const size_t wbytes = 2 * (size_t)(p.Nq + p.Nkv);  // the weights, once per CTA
   for (int w = 4; w <= kStagedMaxWarps; ++w) {
-    const size_t cta = kStagedHeader + w * per_warp + 1024;  // + the per-CTA reservation
+    const size_t cta = kStagedHeader + wbytes + w * per_warp + 1024;  // + the per-CTA reservation
     const int ctas = (int)(budget / cta);
     const int total = ctas * w > 64 ? 64 / w * w : ctas * w;  // 64 warps per SM at most
     if (total > best_total) { best_total = total; best_w = w; }
   }
-  const size_t smem = kStagedHeader + (size_t)best_w * per_warp;
+  const size_t smem = kStagedHeader + wbytes + (size_t)best_w * per_warp;
   cudaError_t e =
       cudaFuncSetAttribute(rmsnorm_mx_tma, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;

@@ -237,3 +237,38 @@ def mx_block(yq):
 def static_quant(x_bits, descale: float):
     d = Fraction(descale)
     return [e4m3_code(rn32(bf16_to_frac(b) / d), (b & 0x8000) != 0) for b in x_bits]
+
+
+def quant_row(y_bits):
+    """Per-token quantisation of a bf16 row: (codes, scale)."""
+    amax = max(abs(bf16_to_frac(b)) for b in y_bits)
+    scale = rn32(amax / 448)
+    codes = []
+    for b in y_bits:
+        neg = (b & 0x8000) != 0
+        codes.append((0x80 if neg else 0) if amax == 0 else e4m3_code(rn32(bf16_to_frac(b) / scale), neg))
+    return codes, scale
+
+
+def gated_quant_row(x_bits, g_bits, act: str, act_tab=None):
+    """y = bf16(x * bf16(act(g))) per element, then the per-token quantisation."""
+    y = []
+    for xb, gb in zip(x_bits, g_bits):
+        g = act_tab[gb] if act_tab else act_exact(gb, act)
+        y.append(bf16_bits(bf16_to_frac(xb) * bf16_to_frac(g), neg_zero=((xb ^ g) & 0x8000) != 0))
+    codes, scale = quant_row(y)
+    return y, codes, scale
+
+
+def head_amax(x_bits):
+    """max |x| over a head's values (finite inputs)."""
+    return max(abs(bf16_to_frac(b)) for b in x_bits)
+
+
+def dynamic_quant(x_bits_head):
+    """descale = RN32(amax / 448) of the head, codes of x / descale (signed
+    zeros for a zero head)."""
+    d = rn32(head_amax(x_bits_head) / 448)
+    if d == 0:
+        return d, [0x80 if b & 0x8000 else 0 for b in x_bits_head]
+    return d, [e4m3_code(rn32(bf16_to_frac(b) / d), (b & 0x8000) != 0) for b in x_bits_head]
