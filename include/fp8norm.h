@@ -3,8 +3,9 @@
  *
  * C ABI.  Every operation takes caller-owned DEVICE pointers, plain sizes and
  * strides (in elements), and the caller's cudaStream_t; it validates its
- * arguments on the host, enqueues exactly one kernel on that stream and
- * returns without synchronising, so the calls can be captured in a CUDA graph.
+ * arguments on the host, enqueues its work on that stream (one kernel; the
+ * dynamic per-head quantisation: a memset and two kernels) and returns
+ * without synchronising, so the calls can be captured in a CUDA graph.
  * The operations allocate no memory and keep no state between calls.
  *
  * Element encodings: bf16 inputs/outputs are bfloat16 bit patterns (uint16);
@@ -98,6 +99,48 @@ fp8n_status fp8n_gated_rmsnorm_quant_token(const void* x, int64_t x_stride, cons
                                            uint32_t* status, fp8n_stream_t stream);
 
 /*
+ * The steps of (A) on their own: the unfused pipeline that (A) replaces, and
+ * the standalone per-token quantiser that other producers feed.
+ *
+ * Source: "[ROCm][Kimi-K3] Fuse gated RMSNorm with per-token FP8 for KDA
+ * o_proj" (vLLM PR 54254): Purpose (gated RMSNorm followed by a standalone
+ * dynamic per-token FP8 quant in the linear; the fused-decode output is
+ * quantised by the per-token quantiser alone) and Profile, "Unfused" (the
+ * gated norm and the per-token quant as two launches, 8.5 us against 4.2 us
+ * fused); the cross-referenced "[ROCm][Kimi-K3] Fuse MLA sigmoid-mul with
+ * per-token FP8 for o_proj" (PR 55043, title only) for the gate product
+ * followed by the per-token quant.  Every rounding is the one of (A), so
+ * fp8n_quant_token(fp8n_gated_rmsnorm_bf16(...)) equals
+ * fp8n_gated_rmsnorm_quant_token(...) bit for bit.
+ */
+
+/* y[t, h*D + d] = the bf16 y of (A), written out instead of quantised.
+ * x, gate, weight, limits: as (A).  y: bf16 [T, H*D], token stride y_stride
+ * (elements, multiple of 8, >= H*D). */
+fp8n_status fp8n_gated_rmsnorm_bf16(const void* x, int64_t x_stride, const void* gate,
+                                    int64_t gate_stride, const void* weight, int64_t T, int32_t H,
+                                    int32_t D, float eps, fp8n_act act, void* y, int64_t y_stride,
+                                    uint32_t* status, fp8n_stream_t stream);
+
+/* Per-token FP8 of bf16 rows: scale[t] = RN32(max_n |y[t,n]| / 448),
+ * out[t, n] = e4m3(RN32(y[t,n] / scale[t])) (zero rows: scale 0, signed zero
+ * codes).  y: bf16 [T, N], token stride y_stride (elements, multiple of 8);
+ * out: e4m3 [T, N], out_stride (bytes, multiple of 8); scale: fp32 [T].
+ * Limits: N a multiple of 8 with 8 <= N <= 16384. */
+fp8n_status fp8n_quant_token(const void* y, int64_t y_stride, int64_t T, int32_t N, void* out,
+                             int64_t out_stride, float* scale, uint32_t* status,
+                             fp8n_stream_t stream);
+
+/* Gate product then per-token FP8: y = bf16(x * bf16(act(gate))) per element
+ * of a token row of N values (no norm), then the quantisation of
+ * fp8n_quant_token.  x, gate: bf16 [T, N] with token strides (elements,
+ * multiples of 8); out, scale, limits: as fp8n_quant_token. */
+fp8n_status fp8n_gated_quant_token(const void* x, int64_t x_stride, const void* gate,
+                                   int64_t gate_stride, int64_t T, int32_t N, fp8n_act act,
+                                   void* out, int64_t out_stride, float* scale, uint32_t* status,
+                                   fp8n_stream_t stream);
+
+/*
  * (B) Fused q/kv RMSNorm: q leaves as MXFP8, kv as normalised bf16.
  *
  * Source: "[ROCm][Perf] FP8 o-projection for DeepSeek-V4.1-Flash MLA on AMD
@@ -129,6 +172,32 @@ fp8n_status fp8n_rmsnorm_quant_mx(const void* q, int64_t q_stride, const void* q
                                   uint32_t* status, fp8n_stream_t stream);
 
 /*
+ * The two steps of (B) on their own.  Source: "[ROCm][Perf] FP8 o-projection
+ * for DeepSeek-V4.1-Flash MLA on AMD MI355X" (vLLM PR 57081), third commit
+ * message: the fused producer is bitwise identical to the unfused path, a
+ * row RMSNorm to bf16 followed by the MXFP8 quantisation of q.  Hence
+ * fp8n_quant_mx(fp8n_rmsnorm_bf16(q)) equals the q outputs of
+ * fp8n_rmsnorm_quant_mx, and fp8n_rmsnorm_bf16(kv) its kv output.
+ */
+
+/* y[m, :] = bf16(bf16(RN32(x * r)) * weight), r over the whole row as in (B).
+ * x: bf16 [M, N], row stride x_stride; weight: bf16 [N]; y: bf16 [M, N], row
+ * stride y_stride (elements, multiples of 8).  Limits: N a multiple of 8 with
+ * 8 <= N <= 16384, eps finite and >= 0. */
+fp8n_status fp8n_rmsnorm_bf16(const void* x, int64_t x_stride, const void* weight, int64_t M,
+                              int32_t N, float eps, void* y, int64_t y_stride, uint32_t* status,
+                              fp8n_stream_t stream);
+
+/* MXFP8 of bf16 rows as given (the block rule of (B) without the norm):
+ * scale[m, b] = E8M0 code of block b of y[m, :], out = e4m3(y * 2^-e).
+ * y: bf16 [M, N] (row stride multiple of 8); out: e4m3 [M, N] (row stride
+ * bytes, multiple of 8); scale: uint8 [M, N/32], row stride scale_stride.
+ * Limits: N a multiple of 32 with 32 <= N <= 16384. */
+fp8n_status fp8n_quant_mx(const void* y, int64_t y_stride, int64_t M, int32_t N, void* out,
+                          int64_t out_stride, uint8_t* scale, int64_t scale_stride,
+                          uint32_t* status, fp8n_stream_t stream);
+
+/*
  * (C) Static per-head FP8 quantisation of packed variable-length Q, K, V.
  *
  * Source: "[ROCm][MLA] Add guarded gfx942 FP8 context prefill" (vLLM PR
@@ -149,7 +218,8 @@ fp8n_status fp8n_rmsnorm_quant_mx(const void* q, int64_t q_stride, const void* q
  *            sequences (NULL allowed).  The map is elementwise, so it is only
  *            carried for the caller's bookkeeping; T is the packed length.
  * outputs  : e4m3, contiguous [T, H, Dqk] / [T, H, Dv].
- * Limits   : Dqk, Dv multiples of 8 in [8, 8192]; H >= 1.
+ * Limits   : Dqk, Dv multiples of 8 in [8, 8192]; 1 <= H <= 256; fewer than
+ *            2^31 16-byte chunks in Q, K and V together.
  */
 fp8n_status fp8n_static_head_quant(const void* q, const void* k, const void* v,
                                    int64_t qk_tok_stride, int64_t qk_head_stride,
@@ -159,6 +229,48 @@ fp8n_status fp8n_static_head_quant(const void* q, const void* k, const void* v,
                                    const int32_t* cu_seqlens, int32_t num_seqs, void* q_out,
                                    void* k_out, void* v_out, uint32_t* status,
                                    fp8n_stream_t stream);
+
+/*
+ * Dynamic per-head FP8 quantisation of packed Q, K, V: the path that the
+ * static quantiser (C) replaces, and the producer of (C)'s descales.
+ *
+ * Source: "[ROCm][MLA] Add guarded gfx942 FP8 context prefill" (vLLM PR
+ * 51551): Summary (static per-head scales remove the dynamic amax
+ * reductions) and the commit messages (dynamic per-head reductions cost work
+ * on every long-context prefill step; dynamic FP8 stays available).
+ *
+ * For each tensor X in (Q, K, V) and head h:
+ *   descale_X[h] = RN32(max_{t,d} |X[t,h,d]| / 448)
+ *   X_out[t,h,d] = e4m3(RN32(X[t,h,d] / descale_X[h]))
+ * A head whose values are all zero gets descale 0 and zero codes carrying the
+ * sign of x; a NaN anywhere in a head makes its descale NaN and its codes
+ * NaN.  Tensors, strides, outputs and limits: as (C).
+ * workspace: device uint32 [3*H], 4-byte aligned, owned by the caller; the
+ *            call zeroes it on the stream and leaves the per-head maxima in it
+ *            (as binary32 bit patterns); calls that share it must not overlap.
+ * q/k/v_descale: fp32 [H] device outputs.
+ * Work enqueued: a memset of the workspace, the max pass, the quantise pass.
+ */
+fp8n_status fp8n_dynamic_head_quant(const void* q, const void* k, const void* v,
+                                    int64_t qk_tok_stride, int64_t qk_head_stride,
+                                    int64_t v_tok_stride, int64_t v_head_stride, int64_t T,
+                                    int32_t H, int32_t Dqk, int32_t Dv, uint32_t* workspace,
+                                    float* q_descale, float* k_descale, float* v_descale,
+                                    void* q_out, void* k_out, void* v_out, fp8n_stream_t stream);
+
+/*
+ * Calibration: running per-head maxima of one packed tensor,
+ *   amax[h] = max(amax[h], max_{t,d} |x[t,h,d]|),
+ * as collected after warm-up to build (C)'s descales.  Source: "[ROCm][MLA]
+ * Add guarded gfx942 FP8 context prefill" (vLLM PR 51551), "What this PR
+ * does" (layer-owned Q/K/V maxima collected after warmup in calibration
+ * mode).  x: bf16 [T, H, Dh] with token and head strides (elements, multiples
+ * of 8); amax: fp32 [H] device, in/out, entries >= +0 on entry (start from
+ * zeros); a NaN in x makes its head's entry NaN.  Limits: Dh a multiple of 8
+ * in [8, 8192], 1 <= H <= 256.
+ */
+fp8n_status fp8n_head_amax(const void* x, int64_t tok_stride, int64_t head_stride, int64_t T,
+                           int32_t H, int32_t Dh, float* amax, fp8n_stream_t stream);
 
 /*
  * Gate activation alone: out[i] = bf16(act(g[i])), act = sigmoid or

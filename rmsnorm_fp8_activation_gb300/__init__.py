@@ -65,6 +65,19 @@ def lib() -> ctypes.CDLL:
         L.fp8n_gate_act_bf16.restype = ctypes.c_int
         L.fp8n_check_descales.argtypes = [P, i32, P]
         L.fp8n_check_descales.restype = ctypes.c_int
+        L.fp8n_gated_rmsnorm_bf16.argtypes = [
+            P, i64, P, i64, P, i64, i32, i32, f32, ctypes.c_int, P, i64, P, P]
+        L.fp8n_quant_token.argtypes = [P, i64, i64, i32, P, i64, P, P, P]
+        L.fp8n_gated_quant_token.argtypes = [P, i64, P, i64, i64, i32, ctypes.c_int, P, i64, P, P, P]
+        L.fp8n_rmsnorm_bf16.argtypes = [P, i64, P, i64, i32, f32, P, i64, P, P]
+        L.fp8n_quant_mx.argtypes = [P, i64, i64, i32, P, i64, P, i64, P, P]
+        L.fp8n_dynamic_head_quant.argtypes = [
+            P, P, P, i64, i64, i64, i64, i64, i32, i32, i32, P, P, P, P, P, P, P, P]
+        L.fp8n_head_amax.argtypes = [P, i64, i64, i64, i32, i32, P, P]
+        for name in ("fp8n_gated_rmsnorm_bf16", "fp8n_quant_token", "fp8n_gated_quant_token",
+                     "fp8n_rmsnorm_bf16", "fp8n_quant_mx", "fp8n_dynamic_head_quant",
+                     "fp8n_head_amax"):
+            getattr(L, name).restype = ctypes.c_int
         _lib = L
     return _lib
 
@@ -202,3 +215,130 @@ def fp8n_check_descales(descale, stream=None) -> bool:
         return False
     _check("fp8n_check_descales", code)
     return True
+
+
+# ---- the steps of (A) and (B) on their own, dynamic per-head quantisation ----
+
+def fp8n_gated_rmsnorm_bf16(x, gate, weight, eps: float = 1e-6, act: int = ACT_SIGMOID, y=None,
+                            status=None, stream=None):
+    """(A) without the quantisation.  x, gate: [T, H, D] bf16; returns y bf16 [T, H*D]."""
+    _need(x, "x", _BF16, 3)
+    _need(gate, "gate", _BF16, 3)
+    _need(weight, "weight", _BF16, 1)
+    T, H, D = x.shape
+    if gate.shape != x.shape or weight.shape[0] != D:
+        raise ValueError("shape mismatch between x, gate and weight")
+    for t, n in ((x, "x"), (gate, "gate")):
+        if t.stride(1) != D:
+            raise ValueError("%s: heads must be contiguous inside a token" % n)
+    if y is None:
+        y = torch.empty((T, H * D), dtype=torch.bfloat16, device=x.device)
+    _need(y, "y", _BF16, 2)
+    _check("fp8n_gated_rmsnorm_bf16", lib().fp8n_gated_rmsnorm_bf16(
+        _ptr(x), x.stride(0), _ptr(gate), gate.stride(0), _ptr(weight), T, H, D, eps, act,
+        _ptr(y), y.stride(0), _ptr(status), _stream(stream)))
+    return y
+
+
+def fp8n_quant_token(y, out=None, scale=None, status=None, stream=None):
+    """Per-token FP8 of bf16 rows y [T, N].  Returns (out uint8 [T, N], scale float32 [T])."""
+    _need(y, "y", _BF16, 2)
+    T, N = y.shape
+    if out is None:
+        out = torch.empty((T, N), dtype=torch.uint8, device=y.device)
+    if scale is None:
+        scale = torch.empty((T,), dtype=torch.float32, device=y.device)
+    _need(out, "out", _U8, 2)
+    _check("fp8n_quant_token", lib().fp8n_quant_token(
+        _ptr(y), y.stride(0), T, N, _ptr(out), out.stride(0), _ptr(scale), _ptr(status),
+        _stream(stream)))
+    return out, scale
+
+
+def fp8n_gated_quant_token(x, gate, act: int = ACT_SIGMOID, out=None, scale=None, status=None,
+                           stream=None):
+    """y = bf16(x * bf16(act(gate))) on rows [T, N], then per-token FP8.
+    Returns (out uint8 [T, N], scale float32 [T])."""
+    _need(x, "x", _BF16, 2)
+    _need(gate, "gate", _BF16, 2)
+    if gate.shape != x.shape:
+        raise ValueError("x and gate must have the same shape")
+    T, N = x.shape
+    if out is None:
+        out = torch.empty((T, N), dtype=torch.uint8, device=x.device)
+    if scale is None:
+        scale = torch.empty((T,), dtype=torch.float32, device=x.device)
+    _need(out, "out", _U8, 2)
+    _check("fp8n_gated_quant_token", lib().fp8n_gated_quant_token(
+        _ptr(x), x.stride(0), _ptr(gate), gate.stride(0), T, N, act, _ptr(out), out.stride(0),
+        _ptr(scale), _ptr(status), _stream(stream)))
+    return out, scale
+
+
+def fp8n_rmsnorm_bf16(x, weight, eps: float = 1e-6, y=None, status=None, stream=None):
+    """Row RMSNorm of bf16 rows x [M, N] with weight [N]: y bf16 [M, N]."""
+    _need(x, "x", _BF16, 2)
+    _need(weight, "weight", _BF16, 1)
+    M, N = x.shape
+    if weight.shape[0] != N:
+        raise ValueError("weight must have one entry per column")
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
+    _need(y, "y", _BF16, 2)
+    _check("fp8n_rmsnorm_bf16", lib().fp8n_rmsnorm_bf16(
+        _ptr(x), x.stride(0), _ptr(weight), M, N, eps, _ptr(y), y.stride(0), _ptr(status),
+        _stream(stream)))
+    return y
+
+
+def fp8n_quant_mx(y, out=None, scale=None, status=None, stream=None):
+    """MXFP8 of bf16 rows y [M, N] (N % 32 == 0).
+    Returns (out uint8 [M, N], scale uint8 E8M0 [M, N/32])."""
+    _need(y, "y", _BF16, 2)
+    M, N = y.shape
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.uint8, device=y.device)
+    if scale is None:
+        scale = torch.empty((M, N // 32), dtype=torch.uint8, device=y.device)
+    _check("fp8n_quant_mx", lib().fp8n_quant_mx(
+        _ptr(y), y.stride(0), M, N, _ptr(out), out.stride(0), _ptr(scale), scale.stride(0),
+        _ptr(status), _stream(stream)))
+    return out, scale
+
+
+def fp8n_dynamic_head_quant(q, k, v, workspace=None, descales=None, q_out=None, k_out=None,
+                            v_out=None, stream=None):
+    """Dynamic per-head FP8 of packed Q [T,H,Dqk], K [T,H,Dqk], V [T,H,Dv] (bf16).
+    Returns ((q_descale, k_descale, v_descale) float32 [H] each, (q_out, k_out, v_out))."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _need(t, n, _BF16, 3)
+    T, H, Dqk = q.shape
+    Dv = v.shape[2]
+    if k.shape != q.shape or v.shape[:2] != (T, H) or k.stride() != q.stride():
+        raise ValueError("q and k must share shape and strides; v must match [T, H]")
+    dev = q.device
+    if workspace is None:
+        workspace = torch.empty((3 * H,), dtype=torch.int32, device=dev)
+    if descales is None:
+        descales = tuple(torch.empty((H,), dtype=torch.float32, device=dev) for _ in range(3))
+    outs = []
+    for o, d in ((q_out, Dqk), (k_out, Dqk), (v_out, Dv)):
+        outs.append(o if o is not None else torch.empty((T, H, d), dtype=torch.uint8, device=dev))
+    _check("fp8n_dynamic_head_quant", lib().fp8n_dynamic_head_quant(
+        _ptr(q), _ptr(k), _ptr(v), q.stride(0), q.stride(1), v.stride(0), v.stride(1), T, H, Dqk,
+        Dv, _ptr(workspace), _ptr(descales[0]), _ptr(descales[1]), _ptr(descales[2]),
+        _ptr(outs[0]), _ptr(outs[1]), _ptr(outs[2]), _stream(stream)))
+    return tuple(descales), tuple(outs)
+
+
+def fp8n_head_amax(x, amax=None, stream=None):
+    """Running per-head max |x| of x [T, H, Dh] (bf16) folded into amax float32 [H]
+    (zeros when not given).  Returns amax."""
+    _need(x, "x", _BF16, 3)
+    T, H, Dh = x.shape
+    if amax is None:
+        amax = torch.zeros((H,), dtype=torch.float32, device=x.device)
+    _need(amax, "amax", (torch.float32,), 1)
+    _check("fp8n_head_amax", lib().fp8n_head_amax(
+        _ptr(x), x.stride(0), x.stride(1), T, H, Dh, _ptr(amax), _stream(stream)))
+    return amax

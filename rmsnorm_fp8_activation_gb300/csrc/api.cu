@@ -49,7 +49,26 @@ const char* fp8n_status_string(fp8n_status s) {
 
 int fp8n_last_cuda_error(void) { return g_last_cuda_error; }
 
-uint32_t fp8n_version(void) { return 0x000100u; }
+uint32_t fp8n_version(void) { return 0x000200u; }
+
+// Shared validation of the per-token family: rows of T tokens, row length
+// `row` = H*D elements; x (and gate when given) bf16 rows; outputs checked by
+// the callers.
+static fp8n_status check_rows(const void* x, int64_t x_stride, const void* gate,
+                              int64_t gate_stride, bool with_gate, int64_t T, int64_t row) {
+  if (x_stride < row || (with_gate && gate_stride < row)) return FP8N_ERR_SHAPE;
+  if (T == 0) return FP8N_OK;
+  if (!x || (with_gate && !gate)) return FP8N_ERR_NULL;
+  if (!aligned16(x) || x_stride % 8 || (with_gate && (!aligned16(gate) || gate_stride % 8)))
+    return FP8N_ERR_MISALIGNED;
+  return FP8N_OK;
+}
+
+static bool bad_eps(float eps) { return !(eps >= 0.0f) || std::isinf(eps); }
+
+static fp8n_status launch_tokens(const fp8n::GatedParams& p, fp8n_stream_t stream) {
+  return cuda_status(fp8n::launch_gated(p, (cudaStream_t)stream));
+}
 
 fp8n_status fp8n_gated_rmsnorm_quant_token(const void* x, int64_t x_stride, const void* gate,
                                            int64_t gate_stride, const void* weight, int64_t T,
@@ -59,16 +78,17 @@ fp8n_status fp8n_gated_rmsnorm_quant_token(const void* x, int64_t x_stride, cons
   if (T < 0 || H < 1 || D < 1) return FP8N_ERR_SHAPE;
   if (act != FP8N_ACT_SIGMOID && act != FP8N_ACT_SILU) return FP8N_ERR_UNSUPPORTED;
   if (D % 8 != 0 || D > 8192 || (int64_t)H * D > 16384) return FP8N_ERR_UNSUPPORTED;
-  if (!(eps >= 0.0f) || std::isinf(eps)) return FP8N_ERR_UNSUPPORTED;
+  if (bad_eps(eps)) return FP8N_ERR_UNSUPPORTED;
   const int64_t row = (int64_t)H * D;
-  if (x_stride < row || gate_stride < row || out_stride < row) return FP8N_ERR_SHAPE;
-  if (T == 0) return FP8N_OK;
-  if (!x || !gate || !weight || !out || !scale) return FP8N_ERR_NULL;
-  if (!aligned16(x) || !aligned16(gate) || !aligned16(weight) || !aligned16(out) ||
-      x_stride % 8 || gate_stride % 8 || out_stride % 8 || ((uintptr_t)scale & 3u) ||
+  if (out_stride < row) return FP8N_ERR_SHAPE;
+  fp8n_status s = check_rows(x, x_stride, gate, gate_stride, true, T, row);
+  if (s != FP8N_OK || T == 0) return s;
+  if (!weight || !out || !scale) return FP8N_ERR_NULL;
+  if (!aligned16(weight) || !aligned16(out) || out_stride % 8 || ((uintptr_t)scale & 3u) ||
       ((uintptr_t)status & 3u))
     return FP8N_ERR_MISALIGNED;
-  fp8n::GatedParams p;
+  fp8n::GatedParams p = {};
+  p.mode = fp8n::kModeNormQuant;
   p.x = (const uint16_t*)x;
   p.x_stride = x_stride;
   p.gate = (const uint16_t*)gate;
@@ -83,7 +103,88 @@ fp8n_status fp8n_gated_rmsnorm_quant_token(const void* x, int64_t x_stride, cons
   p.out_stride = out_stride;
   p.scale = scale;
   p.status = status;
-  return cuda_status(fp8n::launch_gated(p, (cudaStream_t)stream));
+  return launch_tokens(p, stream);
+}
+
+fp8n_status fp8n_gated_rmsnorm_bf16(const void* x, int64_t x_stride, const void* gate,
+                                    int64_t gate_stride, const void* weight, int64_t T, int32_t H,
+                                    int32_t D, float eps, fp8n_act act, void* y, int64_t y_stride,
+                                    uint32_t* status, fp8n_stream_t stream) {
+  if (T < 0 || H < 1 || D < 1) return FP8N_ERR_SHAPE;
+  if (act != FP8N_ACT_SIGMOID && act != FP8N_ACT_SILU) return FP8N_ERR_UNSUPPORTED;
+  if (D % 8 != 0 || D > 8192 || (int64_t)H * D > 16384) return FP8N_ERR_UNSUPPORTED;
+  if (bad_eps(eps)) return FP8N_ERR_UNSUPPORTED;
+  const int64_t row = (int64_t)H * D;
+  if (y_stride < row) return FP8N_ERR_SHAPE;
+  fp8n_status s = check_rows(x, x_stride, gate, gate_stride, true, T, row);
+  if (s != FP8N_OK || T == 0) return s;
+  if (!weight || !y) return FP8N_ERR_NULL;
+  if (!aligned16(weight) || !aligned16(y) || y_stride % 8 || ((uintptr_t)status & 3u))
+    return FP8N_ERR_MISALIGNED;
+  fp8n::GatedParams p = {};
+  p.mode = fp8n::kModeNormOnly;
+  p.x = (const uint16_t*)x;
+  p.x_stride = x_stride;
+  p.gate = (const uint16_t*)gate;
+  p.gate_stride = gate_stride;
+  p.weight = (const uint16_t*)weight;
+  p.T = T;
+  p.H = H;
+  p.D = D;
+  p.eps = eps;
+  p.act = (int)act;
+  p.y_out = (uint16_t*)y;
+  p.y_stride = y_stride;
+  p.status = status;
+  return launch_tokens(p, stream);
+}
+
+// The gate product and the per-token quantisation without the norm, or the
+// quantisation alone (gate == NULL path of the shared body below).
+static fp8n_status token_quant(int mode, const void* x, int64_t x_stride, const void* gate,
+                               int64_t gate_stride, int64_t T, int32_t N, int act, void* out,
+                               int64_t out_stride, float* scale, uint32_t* status,
+                               fp8n_stream_t stream) {
+  if (T < 0 || N < 1) return FP8N_ERR_SHAPE;
+  if (N % 8 != 0 || N > 16384) return FP8N_ERR_UNSUPPORTED;
+  if (out_stride < N) return FP8N_ERR_SHAPE;
+  const bool with_gate = mode == fp8n::kModeGateQuant;
+  fp8n_status s = check_rows(x, x_stride, gate, gate_stride, with_gate, T, N);
+  if (s != FP8N_OK || T == 0) return s;
+  if (!out || !scale) return FP8N_ERR_NULL;
+  if (!aligned16(out) || out_stride % 8 || ((uintptr_t)scale & 3u) || ((uintptr_t)status & 3u))
+    return FP8N_ERR_MISALIGNED;
+  fp8n::GatedParams p = {};
+  p.mode = mode;
+  p.x = (const uint16_t*)x;
+  p.x_stride = x_stride;
+  p.gate = (const uint16_t*)gate;
+  p.gate_stride = gate_stride;
+  p.T = T;
+  p.H = 1;
+  p.D = N;
+  p.act = act;
+  p.out = (uint8_t*)out;
+  p.out_stride = out_stride;
+  p.scale = scale;
+  p.status = status;
+  return launch_tokens(p, stream);
+}
+
+fp8n_status fp8n_gated_quant_token(const void* x, int64_t x_stride, const void* gate,
+                                   int64_t gate_stride, int64_t T, int32_t N, fp8n_act act,
+                                   void* out, int64_t out_stride, float* scale, uint32_t* status,
+                                   fp8n_stream_t stream) {
+  if (act != FP8N_ACT_SIGMOID && act != FP8N_ACT_SILU) return FP8N_ERR_UNSUPPORTED;
+  return token_quant(fp8n::kModeGateQuant, x, x_stride, gate, gate_stride, T, N, (int)act, out,
+                     out_stride, scale, status, stream);
+}
+
+fp8n_status fp8n_quant_token(const void* y, int64_t y_stride, int64_t T, int32_t N, void* out,
+                             int64_t out_stride, float* scale, uint32_t* status,
+                             fp8n_stream_t stream) {
+  return token_quant(fp8n::kModeQuant, y, y_stride, nullptr, 0, T, N, 0, out, out_stride, scale,
+                     status, stream);
 }
 
 fp8n_status fp8n_rmsnorm_quant_mx(const void* q, int64_t q_stride, const void* q_weight,
@@ -106,7 +207,7 @@ fp8n_status fp8n_rmsnorm_quant_mx(const void* q, int64_t q_stride, const void* q
   if (Nkv > 0 && (!aligned16(kv) || !aligned16(kv_weight) || !aligned16(kv_out) ||
                   kv_stride % 8 || kv_out_stride % 8))
     return FP8N_ERR_MISALIGNED;
-  fp8n::MxParams p;
+  fp8n::MxParams p = {};
   p.q = (const uint16_t*)q;
   p.q_stride = q_stride;
   p.q_weight = (const uint16_t*)q_weight;
@@ -127,6 +228,92 @@ fp8n_status fp8n_rmsnorm_quant_mx(const void* q, int64_t q_stride, const void* q
   return cuda_status(fp8n::launch_mx(p, (cudaStream_t)stream));
 }
 
+fp8n_status fp8n_rmsnorm_bf16(const void* x, int64_t x_stride, const void* weight, int64_t M,
+                              int32_t N, float eps, void* y, int64_t y_stride, uint32_t* status,
+                              fp8n_stream_t stream) {
+  if (M < 0 || N < 1) return FP8N_ERR_SHAPE;
+  if (N % 8 != 0 || N > 16384 || bad_eps(eps)) return FP8N_ERR_UNSUPPORTED;
+  if (x_stride < N || y_stride < N) return FP8N_ERR_SHAPE;
+  if (M == 0) return FP8N_OK;
+  if (!x || !weight || !y) return FP8N_ERR_NULL;
+  if (!aligned16(x) || !aligned16(weight) || !aligned16(y) || x_stride % 8 || y_stride % 8 ||
+      ((uintptr_t)status & 3u))
+    return FP8N_ERR_MISALIGNED;
+  fp8n::MxParams p = {};  // no q columns: the kv path of (B) alone
+  p.kv = (const uint16_t*)x;
+  p.kv_stride = x_stride;
+  p.kv_weight = (const uint16_t*)weight;
+  p.Nkv = N;
+  p.M = M;
+  p.eps = eps;
+  p.kv_out = (uint16_t*)y;
+  p.kv_out_stride = y_stride;
+  p.status = status;
+  return cuda_status(fp8n::launch_mx(p, (cudaStream_t)stream));
+}
+
+fp8n_status fp8n_quant_mx(const void* y, int64_t y_stride, int64_t M, int32_t N, void* out,
+                          int64_t out_stride, uint8_t* scale, int64_t scale_stride,
+                          uint32_t* status, fp8n_stream_t stream) {
+  if (M < 0 || N < 1) return FP8N_ERR_SHAPE;
+  if (N % 32 != 0 || N > 16384) return FP8N_ERR_UNSUPPORTED;
+  if (y_stride < N || out_stride < N || scale_stride < N / 32) return FP8N_ERR_SHAPE;
+  if (M == 0) return FP8N_OK;
+  if (!y || !out || !scale) return FP8N_ERR_NULL;
+  if (!aligned16(y) || !aligned16(out) || y_stride % 8 || out_stride % 8 ||
+      ((uintptr_t)status & 3u))
+    return FP8N_ERR_MISALIGNED;
+  fp8n::MxParams p = {};  // q taken as already normalised, no kv columns
+  p.q = (const uint16_t*)y;
+  p.q_stride = y_stride;
+  p.Nq = N;
+  p.M = M;
+  p.q_out = (uint8_t*)out;
+  p.q_out_stride = out_stride;
+  p.q_scale = scale;
+  p.q_scale_stride = scale_stride;
+  p.q_prenorm = 1;
+  p.status = status;
+  return cuda_status(fp8n::launch_mx(p, (cudaStream_t)stream));
+}
+
+// Shared validation of the packed Q/K/V calls (descale pointers checked by
+// the callers); fills the tensors of p.
+static fp8n_status check_qkv(const void* q, const void* k, const void* v, int64_t qk_tok_stride,
+                             int64_t qk_head_stride, int64_t v_tok_stride, int64_t v_head_stride,
+                             int64_t T, int32_t H, int32_t Dqk, int32_t Dv, void* q_out,
+                             void* k_out, void* v_out, fp8n::StaticParams* p) {
+  if (T < 0 || H < 1 || Dqk < 1 || Dv < 1) return FP8N_ERR_SHAPE;
+  if (Dqk % 8 || Dv % 8 || Dqk > 8192 || Dv > 8192 || H > 256) return FP8N_ERR_UNSUPPORTED;
+  if (qk_head_stride < Dqk || v_head_stride < Dv || qk_tok_stride < 0 || v_tok_stride < 0)
+    return FP8N_ERR_SHAPE;
+  // one launch addresses every chunk with 32-bit indices
+  const int64_t chunks = T * H * (int64_t)(2 * Dqk + Dv) / 8;
+  if (chunks >= (int64_t)1 << 31) return FP8N_ERR_UNSUPPORTED;
+  if (T == 0) return FP8N_OK;
+  if (!q || !k || !v || !q_out || !k_out || !v_out) return FP8N_ERR_NULL;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(q_out) || !aligned16(k_out) ||
+      !aligned16(v_out) || qk_tok_stride % 8 || qk_head_stride % 8 || v_tok_stride % 8 ||
+      v_head_stride % 8)
+    return FP8N_ERR_MISALIGNED;
+  const void* in[3] = {q, k, v};
+  void* out[3] = {q_out, k_out, v_out};
+  for (int i = 0; i < 3; ++i) {
+    p->t[i].x = (const uint16_t*)in[i];
+    p->t[i].tok_stride = i < 2 ? qk_tok_stride : v_tok_stride;
+    p->t[i].head_stride = i < 2 ? qk_head_stride : v_head_stride;
+    p->t[i].Dh = i < 2 ? Dqk : Dv;
+    p->t[i].descale = nullptr;
+    p->t[i].out = (uint8_t*)out[i];
+  }
+  p->T = T;
+  p->H = H;
+  p->status = nullptr;
+  return FP8N_OK;
+}
+
+static bool misaligned4(const void* p) { return ((uintptr_t)p & 3u) != 0; }
+
 fp8n_status fp8n_static_head_quant(const void* q, const void* k, const void* v,
                                    int64_t qk_tok_stride, int64_t qk_head_stride,
                                    int64_t v_tok_stride, int64_t v_head_stride, int64_t T,
@@ -136,37 +323,61 @@ fp8n_status fp8n_static_head_quant(const void* q, const void* k, const void* v,
                                    void* k_out, void* v_out, uint32_t* status,
                                    fp8n_stream_t stream) {
   (void)cu_seqlens;
-  if (T < 0 || H < 1 || Dqk < 1 || Dv < 1 || num_seqs < 0) return FP8N_ERR_SHAPE;
-  if (Dqk % 8 || Dv % 8 || Dqk > 8192 || Dv > 8192 || H > 256) return FP8N_ERR_UNSUPPORTED;
-  if (qk_head_stride < Dqk || v_head_stride < Dv || qk_tok_stride < 0 || v_tok_stride < 0)
-    return FP8N_ERR_SHAPE;
-  // one launch addresses every chunk with 32-bit indices
-  const int64_t chunks = T * H * (int64_t)(2 * Dqk + Dv) / 8;
-  if (chunks >= (int64_t)1 << 31) return FP8N_ERR_UNSUPPORTED;
-  if (T == 0) return FP8N_OK;
-  if (!q || !k || !v || !q_descale || !k_descale || !v_descale || !q_out || !k_out || !v_out)
-    return FP8N_ERR_NULL;
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(q_out) || !aligned16(k_out) ||
-      !aligned16(v_out) || qk_tok_stride % 8 || qk_head_stride % 8 || v_tok_stride % 8 ||
-      v_head_stride % 8 || ((uintptr_t)q_descale & 3u) || ((uintptr_t)k_descale & 3u) ||
-      ((uintptr_t)v_descale & 3u) || ((uintptr_t)status & 3u))
+  if (num_seqs < 0) return FP8N_ERR_SHAPE;
+  fp8n::StaticParams p = {};
+  fp8n_status s = check_qkv(q, k, v, qk_tok_stride, qk_head_stride, v_tok_stride, v_head_stride,
+                            T, H, Dqk, Dv, q_out, k_out, v_out, &p);
+  if (s != FP8N_OK || T == 0) return s;
+  if (!q_descale || !k_descale || !v_descale) return FP8N_ERR_NULL;
+  if (misaligned4(q_descale) || misaligned4(k_descale) || misaligned4(v_descale) ||
+      misaligned4(status))
     return FP8N_ERR_MISALIGNED;
-  fp8n::StaticParams p;
-  const void* in[3] = {q, k, v};
-  void* out[3] = {q_out, k_out, v_out};
   const float* d[3] = {q_descale, k_descale, v_descale};
-  for (int i = 0; i < 3; ++i) {
-    p.t[i].x = (const uint16_t*)in[i];
-    p.t[i].tok_stride = i < 2 ? qk_tok_stride : v_tok_stride;
-    p.t[i].head_stride = i < 2 ? qk_head_stride : v_head_stride;
-    p.t[i].Dh = i < 2 ? Dqk : Dv;
-    p.t[i].descale = d[i];
-    p.t[i].out = (uint8_t*)out[i];
-  }
-  p.T = T;
-  p.H = H;
+  for (int i = 0; i < 3; ++i) p.t[i].descale = d[i];
   p.status = status;
   return cuda_status(fp8n::launch_static(p, (cudaStream_t)stream));
+}
+
+fp8n_status fp8n_dynamic_head_quant(const void* q, const void* k, const void* v,
+                                    int64_t qk_tok_stride, int64_t qk_head_stride,
+                                    int64_t v_tok_stride, int64_t v_head_stride, int64_t T,
+                                    int32_t H, int32_t Dqk, int32_t Dv, uint32_t* workspace,
+                                    float* q_descale, float* k_descale, float* v_descale,
+                                    void* q_out, void* k_out, void* v_out, fp8n_stream_t stream) {
+  fp8n::DynamicParams p = {};
+  fp8n_status s = check_qkv(q, k, v, qk_tok_stride, qk_head_stride, v_tok_stride, v_head_stride,
+                            T, H, Dqk, Dv, q_out, k_out, v_out, &p.s);
+  if (s != FP8N_OK || T == 0) return s;
+  if (!workspace || !q_descale || !k_descale || !v_descale) return FP8N_ERR_NULL;
+  if (misaligned4(workspace) || misaligned4(q_descale) || misaligned4(k_descale) ||
+      misaligned4(v_descale))
+    return FP8N_ERR_MISALIGNED;
+  p.descale_out[0] = q_descale;
+  p.descale_out[1] = k_descale;
+  p.descale_out[2] = v_descale;
+  p.amax_bits = workspace;
+  return cuda_status(fp8n::launch_dynamic(p, (cudaStream_t)stream));
+}
+
+fp8n_status fp8n_head_amax(const void* x, int64_t tok_stride, int64_t head_stride, int64_t T,
+                           int32_t H, int32_t Dh, float* amax, fp8n_stream_t stream) {
+  if (T < 0 || H < 1 || Dh < 1) return FP8N_ERR_SHAPE;
+  if (Dh % 8 || Dh > 8192 || H > 256) return FP8N_ERR_UNSUPPORTED;
+  if (head_stride < Dh || tok_stride < 0) return FP8N_ERR_SHAPE;
+  if (T * H * (int64_t)Dh / 8 >= (int64_t)1 << 31) return FP8N_ERR_UNSUPPORTED;
+  if (T == 0) return FP8N_OK;
+  if (!x || !amax) return FP8N_ERR_NULL;
+  if (!aligned16(x) || tok_stride % 8 || head_stride % 8 || misaligned4(amax))
+    return FP8N_ERR_MISALIGNED;
+  fp8n::AmaxParams p = {};
+  p.x = (const uint16_t*)x;
+  p.tok_stride = tok_stride;
+  p.head_stride = head_stride;
+  p.T = T;
+  p.H = H;
+  p.Dh = Dh;
+  p.amax = amax;
+  return cuda_status(fp8n::launch_head_amax(p, (cudaStream_t)stream));
 }
 
 fp8n_status fp8n_gate_act_bf16(const void* g, int64_t n, fp8n_act act, void* out,

@@ -15,11 +15,27 @@
 // thread and a double-float butterfly over those lanes.  y stays in registers
 // as bf16 pairs; the row amax needs one CTA barrier per token, after which the
 // stage is refilled and the codes are written with 8-byte stores.
+//
+// The same kernels, specialised at compile time, also run the steps of (A) on
+// their own (the unfused pipeline): the gated norm to bf16 without the
+// quantisation, and the per-token quantisation of a bf16 row with or without
+// the gate product in front of it.
 #include "common.cuh"
 #include "kernels.h"
 
 namespace fp8n {
 namespace {
+
+// What a compile-time mode computes: y from x alone (kModeQuant), from x and
+// the gate (kModeGateQuant), or through the per-head norm (kModeNormQuant,
+// kModeNormOnly); then codes and scales, or (kModeNormOnly) y itself.
+template <int MODE>
+struct ModeOf {
+  static constexpr bool norm = MODE == kModeNormQuant || MODE == kModeNormOnly;
+  static constexpr bool gate = MODE != kModeQuant;
+  static constexpr bool quant = MODE != kModeNormOnly;
+  static constexpr int nsrc = gate ? 2 : 1;  // rows staged per token
+};
 
 constexpr int kHeader = 1024;  // mbarriers at 0, amax partials at 64
 
@@ -122,15 +138,17 @@ __device__ __forceinline__ void lut_chunk(const uint8_t* lut, const uint32_t g[4
 // Token quantiser: code = e4m3(RN32(y / scale)), from the correctly rounded
 // reciprocal and one FMA correction on packed pairs.  It is arranged on -y
 // (q0 = (-y)*(-1/s), e = q0*s - y, q = q0 - e/s) so that the signs of zero
-// quotients survive.  A zero scale gives signed zero codes.  A scale below
-// 2^-126 (all |y| tiny) has no finite binary32 reciprocal, so y and the scale
-// are both multiplied by 2^64 first: exact scalings that keep the quotient.
+// quotients survive.  A zero scale gives signed zero codes.  The correction is
+// exact while the residual e does not underflow, which holds for every
+// quotient that can reach a nonzero code (|q| >= 2^-11) once s >= 2^-60;
+// smaller scales (|y| tiny) first multiply y and the scale by 2^64, an exact
+// rescaling that keeps the quotient.
 struct TokenQuant {
   f2_t s2, nrs2;
   bool zero, tiny;
   __device__ __forceinline__ TokenQuant(float s) {
     zero = (s == 0.0f);
-    tiny = (s > 0.0f) && (s < 0x1p-126f);
+    tiny = (s > 0.0f) && (s < 0x1p-60f);
     const float sc = tiny ? __fmul_rn(s, 0x1p64f) : s;
     s2 = splat2(sc);
     nrs2 = splat2(-__frcp_rn(sc));
@@ -151,12 +169,23 @@ struct TokenQuant {
   }
 };
 
-template <int ACT, int CPT, int TPH, bool LUT>
+// The exact mean square of the heads flagged in a warp: every lane sums its
+// `count` chunks at p in double-double, the TPH lanes of a head combine their
+// sums, and a flagged lane steps ms to RN32(S / D).  Called by the whole warp.
+static __device__ __noinline__ float head_ms_exact(const uint4* p, int count, int tph, int D,
+                                                   float ms, bool flagged) {
+  dd Sd = sumsq_dd(p, 1, count);
+  for (int m = 1; m < tph; m <<= 1) Sd = dd_add(Sd, shfl_xor_dd(Sd, m));
+  return flagged ? ms_resolve(Sd, (float)D, ms) : ms;
+}
+
+template <int MODE, int ACT, int CPT, int TPH, bool LUT>
 __global__ void __launch_bounds__(512) gated_token_tma(const GatedParams p, int nstage) {
+  using M = ModeOf<MODE>;
   extern __shared__ __align__(1024) uint8_t smem[];
   const int row = p.H * p.D;
   const uint32_t row_bytes = 2u * (uint32_t)row;
-  const uint32_t stage_bytes = 2u * row_bytes;
+  const uint32_t stage_bytes = M::nsrc * row_bytes;
   const int nthr = row / (8 * CPT);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
   const bool active = tid < nthr;
@@ -164,10 +193,11 @@ __global__ void __launch_bounds__(512) gated_token_tma(const GatedParams p, int 
   float* red = reinterpret_cast<float*>(smem + 64);
   uint8_t* lut = smem + kHeader;  // at a fixed offset: its base folds into the loads
   uint16_t* wsm = reinterpret_cast<uint16_t*>(smem + kHeader + (LUT ? kLutBytes : 0));  // weight [D]
-  uint8_t* stages = smem + kHeader + (LUT ? kLutBytes : 0) + 2 * p.D;
+  uint8_t* stages = smem + kHeader + (LUT ? kLutBytes : 0) + (M::norm ? 2 * p.D : 0);
 
-  for (int i = tid; i < p.D / 8; i += blockDim.x)
-    reinterpret_cast<uint4*>(wsm)[i] = reinterpret_cast<const uint4*>(p.weight)[i];
+  if (M::norm)
+    for (int i = tid; i < p.D / 8; i += blockDim.x)
+      reinterpret_cast<uint4*>(wsm)[i] = reinterpret_cast<const uint4*>(p.weight)[i];
   if (tid == 0) {
     for (int s = 0; s < nstage; ++s) mbar_init(smem_u32(&bars[s]), 1);
     asm volatile("fence.mbarrier_init.release.cluster;\n fence.proxy.async.shared::cta;" ::: "memory");
@@ -179,7 +209,7 @@ __global__ void __launch_bounds__(512) gated_token_tma(const GatedParams p, int 
     uint32_t dst = smem_u32(stages + (size_t)s * stage_bytes);
     mbar_expect_tx(bar, stage_bytes);
     bulk_g2s(dst, p.x + t * p.x_stride, row_bytes, bar);
-    bulk_g2s(dst + row_bytes, p.gate + t * p.gate_stride, row_bytes, bar);
+    if (M::gate) bulk_g2s(dst + row_bytes, p.gate + t * p.gate_stride, row_bytes, bar);
   };
   if (tid == 0)
     for (int s = 0; s < nstage; ++s) {
@@ -194,6 +224,12 @@ __global__ void __launch_bounds__(512) gated_token_tma(const GatedParams p, int 
   const int seg = tid * 8 * CPT;  // first element of the thread's segment
   const uint16_t* wseg = wsm + (seg % p.D);
   const float inv_d = 1.0f / (float)p.D;  // exact: D is a power of two here
+  // error bound of a head's sum relative to S, plus the squares below 2^-126
+  // that binary32 rounds (at most 2^-150 each)
+  int lg = 0;
+  while ((1 << lg) < TPH) ++lg;
+  const float rel_err = sumsq_rel_err(4 * CPT, 1 + lg);
+  const float sq_floor = (float)p.D * 0x1p-149f;
 
   int it = 0;
   bool timeout = false;
@@ -204,21 +240,37 @@ __global__ void __launch_bounds__(512) gated_token_tma(const GatedParams p, int 
     const uint8_t* sg = sx + row_bytes;
 
     // pass 1: the head's sum of squares (x is read again in pass 2)
-    kahan2 acc;
+    float ms = 0.0f;
+    if (M::norm) {
+      sumsq2 acc;
 #pragma unroll
-    for (int c = 0; c < CPT; ++c) {
-      const uint4 xv = active ? *reinterpret_cast<const uint4*>(sx + 16 * slot_of<CPT>(c, tid))
-                              : make_uint4(0, 0, 0, 0);
-      const uint32_t* xw = &xv.x;
+      for (int c = 0; c < CPT; ++c) {
+        const uint4 xv = active ? *reinterpret_cast<const uint4*>(sx + 16 * slot_of<CPT>(c, tid))
+                                : make_uint4(0, 0, 0, 0);
+        const uint32_t* xw = &xv.x;
 #pragma unroll
-      for (int k = 0; k < 4; ++k) acc.add_sq(xw[k]);
+        for (int k = 0; k < 4; ++k) acc.add_sq(xw[k]);
+      }
+      df S = acc.value();
+#pragma unroll
+      for (int m = 1; m < TPH; m <<= 1) S = df_add(S, shfl_xor_df(S, m));
+      // RN32(S) is decided when it is the same at both ends of S's error
+      // interval (RN is monotone; the probes' own roundings are far below
+      // err).  S.h == 0 means every square is at most 2^-150, and then so is
+      // S / D: its rounding is 0.  The lanes of a head agree on S, so a head
+      // is flagged as a whole; the rare warp with a flagged head settles it
+      // from a double-double sum over the row.
+      const float err = __fmaf_rn(S.h, rel_err, sq_floor);
+      const float q = __fadd_rn(S.h, S.l);
+      ms = __fmul_rn(q, inv_d);
+      const bool unsure =
+          S.h != 0.0f && __fadd_rn(S.h, __fadd_rn(S.l, err)) != __fadd_rn(S.h, __fsub_rn(S.l, err));
+      if (__any_sync(0xFFFFFFFFu, unsure))
+        ms = head_ms_exact(reinterpret_cast<const uint4*>(sx), active ? CPT : 0, TPH, p.D, ms, unsure);
     }
-    df S = acc.value();
-#pragma unroll
-    for (int m = 1; m < TPH; m <<= 1) S = df_add(S, shfl_xor_df(S, m));
-    const f2_t r2 = splat2(rms_factor(__fmul_rn(__fadd_rn(S.h, S.l), inv_d), p.eps));
 
-    // pass 2: y = bf16(bf16(bf16(x r) w) act(g)), kept as bf16 pairs
+    // pass 2: y (= bf16(bf16(bf16(x r) w) act(g)) through the norm), kept as bf16 pairs
+    const f2_t r2 = splat2(M::norm ? rms_factor(ms, p.eps) : 1.0f);
     uint32_t y[CPT][4];
     uint32_t am2 = 0;
 #pragma unroll
@@ -227,33 +279,57 @@ __global__ void __launch_bounds__(512) gated_token_tma(const GatedParams p, int 
       uint4 xv = make_uint4(0, 0, 0, 0), gv = xv;
       if (active) {
         xv = *reinterpret_cast<const uint4*>(sx + off);
-        gv = *reinterpret_cast<const uint4*>(sg + off);
+        if (M::gate) gv = *reinterpret_cast<const uint4*>(sg + off);
       }
-      const uint4 wv = *reinterpret_cast<const uint4*>(wseg + 8 * slot_of<CPT>(c, tid));
-      const uint32_t *xw = &xv.x, *gw = &gv.x, *ww = &wv.x;
+      const uint32_t *xw = &xv.x, *gw = &gv.x;
       uint32_t ga[4];
-      if (LUT) {
-        lut_chunk<ACT>(lut, gw, ga);
+      if (M::gate) {
+        if (LUT) {
+          lut_chunk<ACT>(lut, gw, ga);
+        } else {
+#pragma unroll
+          for (int k = 0; k < 4; ++k) ga[k] = act_bf16_pair(gw[k], ACT);
+        }
+      }
+      if (M::norm) {
+        const uint4 wv = *reinterpret_cast<const uint4*>(wseg + 8 * slot_of<CPT>(c, tid));
+        const uint32_t* ww = &wv.x;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) y[c][k] = gated_pair(xw[k], ga[k], ww[k], r2);
+      } else if (M::gate) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) y[c][k] = mul_bf16x2(xw[k], ga[k]);
       } else {
 #pragma unroll
-        for (int k = 0; k < 4; ++k) ga[k] = act_bf16_pair(gw[k], ACT);
+        for (int k = 0; k < 4; ++k) y[c][k] = xw[k];
       }
+      if (M::quant) {
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        y[c][k] = gated_pair(xw[k], ga[k], ww[k], r2);
-        am2 = amax_step(am2, y[c][k]);
+        for (int k = 0; k < 4; ++k) am2 = amax_step(am2, y[c][k]);
       }
     }
-    float amax = fmax_nan(bf16_lo(am2), bf16_hi(am2));
-#pragma unroll
-    for (int m = 16; m >= 1; m >>= 1) amax = fmax_nan(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, m));
     float* redb = red + (it & 1) * 32;
-    if (lane == 0) redb[warp] = amax;
+    if (M::quant) {
+      float amax = fmax_nan(bf16_lo(am2), bf16_hi(am2));
+#pragma unroll
+      for (int m = 16; m >= 1; m >>= 1) amax = fmax_nan(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, m));
+      if (lane == 0) redb[warp] = amax;
+    }
     // every thread is done with stage s and has published its warp's amax
     if (__syncthreads_or(timeout)) break;
     if (tid == 0) {
       const int64_t tn = t + (int64_t)nstage * gridDim.x;
       if (tn < p.T) issue(s, tn);
+    }
+    if (!M::quant) {
+      if (active) {
+        uint16_t* yrow = p.y_out + t * p.y_stride + seg;
+#pragma unroll
+        for (int c = 0; c < CPT; ++c)
+          *reinterpret_cast<uint4*>(yrow + 8 * slot_of<CPT>(c, tid)) =
+              make_uint4(y[c][0], y[c][1], y[c][2], y[c][3]);
+      }
+      continue;
     }
     float tam = redb[0];
     for (int w = 1; w < nwarps; ++w) tam = fmax_nan(tam, redb[w]);
@@ -286,9 +362,11 @@ __global__ void __launch_bounds__(512) gated_token_tma(const GatedParams p, int 
 
 // Any D that is a multiple of 8: one CTA per token, three passes over the
 // (cache-resident) row: chunk sums of squares, then y and the amax, then y
-// again and the codes.  Used for head sizes the staged kernel does not take.
-template <int ACT>
+// again and the codes (or, without the quantisation, y itself).  Used for
+// head sizes and row lengths the staged kernel does not take.
+template <int MODE, int ACT>
 __global__ void __launch_bounds__(256) gated_token_generic(const GatedParams p) {
+  using M = ModeOf<MODE>;
   extern __shared__ __align__(1024) uint8_t smem[];
   const int row = p.H * p.D, nch = row / 8, cph = p.D / 8;
   df* part = reinterpret_cast<df*>(smem);
@@ -300,33 +378,68 @@ __global__ void __launch_bounds__(256) gated_token_generic(const GatedParams p) 
   for (int64_t t = blockIdx.x; t < p.T; t += gridDim.x) {
     const uint16_t* xrow = p.x + t * p.x_stride;
     const uint16_t* grow = p.gate + t * p.gate_stride;
-    for (int c = tid; c < nch; c += blockDim.x) {
-      const uint4 v = *reinterpret_cast<const uint4*>(xrow + 8 * c);
-      kahan2 acc;
-      const uint32_t* w = &v.x;
+    if (M::norm) {
+      for (int c = tid; c < nch; c += blockDim.x) {
+        const uint4 v = *reinterpret_cast<const uint4*>(xrow + 8 * c);
+        sumsq2 acc;
+        const uint32_t* w = &v.x;
 #pragma unroll
-      for (int k = 0; k < 4; ++k) acc.add_sq(w[k]);
-      part[c] = acc.value();
-    }
-    __syncthreads();
-    for (int h = warp; h < p.H; h += nwarps) {
-      df S = {0.0f, 0.0f};
-      for (int c = lane; c < cph; c += 32) S = df_add(S, part[h * cph + c]);
+        for (int k = 0; k < 4; ++k) acc.add_sq(w[k]);
+        part[c] = acc.value();
+      }
+      __syncthreads();
+      for (int h = warp; h < p.H; h += nwarps) {  // warp-uniform: one head per warp
+        df S = {0.0f, 0.0f};
+        for (int c = lane; c < cph; c += 32) S = df_add(S, part[h * cph + c]);
 #pragma unroll
-      for (int m = 16; m >= 1; m >>= 1) S = df_add(S, shfl_xor_df(S, m));
-      if (lane == 0) rf[h] = rms_factor(mean_from_sum(S, n, 0.0f, false), p.eps);
+        for (int m = 16; m >= 1; m >>= 1) S = df_add(S, shfl_xor_df(S, m));
+        float ms = mean_from_sum(S, n, 0.0f, false);
+        const float err = __fmaf_rn(S.h, sumsq_rel_err(4, (cph + 31) / 32 + 6), n * 0x1p-149f);
+        const bool unsure = ms_uncertain(S, n, ms, err);
+        if (__any_sync(0xFFFFFFFFu, unsure)) {
+          const int cnt = lane < cph ? (cph - lane + 31) / 32 : 0;
+          dd Sd = sumsq_dd(reinterpret_cast<const uint4*>(xrow + (size_t)h * p.D) + lane, 32, cnt);
+#pragma unroll
+          for (int m = 16; m >= 1; m >>= 1) Sd = dd_add(Sd, shfl_xor_dd(Sd, m));
+          if (unsure) ms = ms_resolve(Sd, n, ms);
+        }
+        if (lane == 0) rf[h] = rms_factor(ms, p.eps);
+      }
+      __syncthreads();
     }
-    __syncthreads();
 
     auto y_chunk = [&](int c, uint32_t y[4]) {
       const uint4 xv = *reinterpret_cast<const uint4*>(xrow + 8 * c);
-      const uint4 gv = *reinterpret_cast<const uint4*>(grow + 8 * c);
-      const uint4 wv = *reinterpret_cast<const uint4*>(p.weight + 8 * (c % cph));
-      const f2_t r2 = splat2(rf[c / cph]);
-      const uint32_t *xw = &xv.x, *gw = &gv.x, *ww = &wv.x;
+      const uint32_t* xw = &xv.x;
+      if (!M::gate) {
 #pragma unroll
-      for (int k = 0; k < 4; ++k) y[k] = gated_pair(xw[k], act_bf16_pair(gw[k], ACT), ww[k], r2);
+        for (int k = 0; k < 4; ++k) y[k] = xw[k];
+        return;
+      }
+      const uint4 gv = *reinterpret_cast<const uint4*>(grow + 8 * c);
+      const uint32_t* gw = &gv.x;
+      if (M::norm) {
+        const uint4 wv = *reinterpret_cast<const uint4*>(p.weight + 8 * (c % cph));
+        const f2_t r2 = splat2(rf[c / cph]);
+        const uint32_t* ww = &wv.x;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) y[k] = gated_pair(xw[k], act_bf16_pair(gw[k], ACT), ww[k], r2);
+      } else {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) y[k] = mul_bf16x2(xw[k], act_bf16_pair(gw[k], ACT));
+      }
     };
+
+    if (!M::quant) {
+      uint16_t* yrow = p.y_out + t * p.y_stride;
+      for (int c = tid; c < nch; c += blockDim.x) {
+        uint32_t y[4];
+        y_chunk(c, y);
+        *reinterpret_cast<uint4*>(yrow + 8 * c) = make_uint4(y[0], y[1], y[2], y[3]);
+      }
+      __syncthreads();  // part / rf are reused by the next token
+      continue;
+    }
 
     uint32_t am2 = 0;
     for (int c = tid; c < nch; c += blockDim.x) {
@@ -355,20 +468,22 @@ __global__ void __launch_bounds__(256) gated_token_generic(const GatedParams p) 
   }
 }
 
-// Rows of 16 KB or more get one stage per CTA, so that four CTAs fit on an SM
-// and the loads of the others overlap each CTA's compute (its own next row
-// also lands while it quantises); shorter rows get two stages.  The gate
-// table is used when each CTA walks enough tokens to pay for filling it.  The
-// grid is the SM count times the CTAs that fit.
-template <int ACT, int CPT, int TPH, bool LUT>
+// Rows of 16 KB or more per stage get one stage per CTA, so that four CTAs
+// fit on an SM and the loads of the others overlap each CTA's compute (its own
+// next row also lands while it quantises); shorter rows get two stages.  The
+// gate table is used when each CTA walks enough tokens to pay for filling it.
+// The grid is the SM count times the CTAs that fit.
+template <int MODE, int ACT, int CPT, int TPH, bool LUT>
 cudaError_t launch_tma_v(const GatedParams& p, cudaStream_t stream) {
-  auto kern = gated_token_tma<ACT, CPT, TPH, LUT>;
+  using M = ModeOf<MODE>;
+  auto kern = gated_token_tma<MODE, ACT, CPT, TPH, LUT>;
   const int row = p.H * p.D;
   const int nthr = row / (8 * CPT);
   const int block = (nthr + 31) / 32 * 32;
-  const size_t stage_bytes = 4u * (size_t)row;
+  const size_t stage_bytes = 2u * M::nsrc * (size_t)row;
   const int nstage = stage_bytes >= 32 * 1024 ? 1 : 2;
-  const size_t smem = kHeader + 2 * (size_t)p.D + (LUT ? kLutBytes : 0) + nstage * stage_bytes;
+  const size_t smem =
+      kHeader + (M::norm ? 2 * (size_t)p.D : 0) + (LUT ? kLutBytes : 0) + nstage * stage_bytes;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   int per_sm = 0;
@@ -381,17 +496,20 @@ cudaError_t launch_tma_v(const GatedParams& p, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
-template <int ACT, int CPT, int TPH>
+template <int MODE, int ACT, int CPT, int TPH>
 cudaError_t launch_tma(const GatedParams& p, cudaStream_t stream) {
-  // the table costs about as much as 8192 / (H*D) tokens of activations per CTA
-  const int64_t per_cta = p.T / ((int64_t)sm_count() * 4);
-  if (per_cta * p.H * p.D >= 8 * kLutEntries) return launch_tma_v<ACT, CPT, TPH, true>(p, stream);
-  return launch_tma_v<ACT, CPT, TPH, false>(p, stream);
+  if (ModeOf<MODE>::gate) {
+    // the table costs about as much as 8192 / (H*D) tokens of activations per CTA
+    const int64_t per_cta = p.T / ((int64_t)sm_count() * 4);
+    if (per_cta * p.H * p.D >= 8 * kLutEntries)
+      return launch_tma_v<MODE, ACT, CPT, TPH, true>(p, stream);
+  }
+  return launch_tma_v<MODE, ACT, CPT, TPH, false>(p, stream);
 }
 
-template <int ACT>
+template <int MODE, int ACT>
 cudaError_t launch_generic(const GatedParams& p, cudaStream_t stream) {
-  auto kern = gated_token_generic<ACT>;
+  auto kern = gated_token_generic<MODE, ACT>;
   const int row = p.H * p.D;
   const size_t smem = (size_t)(row / 8) * sizeof(df) + (size_t)p.H * 4 + 32 * 4;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -406,9 +524,16 @@ cudaError_t launch_generic(const GatedParams& p, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
-template <int ACT>
+template <int MODE, int ACT>
 cudaError_t dispatch(const GatedParams& p, cudaStream_t stream) {
   const int row = p.H * p.D;
+  if (!ModeOf<MODE>::norm) {
+    // no per-head reduction: the staged kernel takes any row of whole
+    // 32-element chunks (four per thread) that fits one CTA and a stage
+    if (row % 32 == 0 && row / 32 <= 512 && 2 * ModeOf<MODE>::nsrc * row <= 64 * 1024)
+      return launch_tma<MODE, ACT, 4, 1>(p, stream);
+    return launch_generic<MODE, ACT>(p, stream);
+  }
   // staged kernel: D/8 a power of two, a head spans at most a warp, the row
   // fits one CTA and a stage fits shared memory
   const int cpt = p.D >= 32 ? 4 : p.D / 8;
@@ -416,24 +541,36 @@ cudaError_t dispatch(const GatedParams& p, cudaStream_t stream) {
   const bool pow2 = (p.D & (p.D - 1)) == 0;
   if (pow2 && tph >= 1 && tph <= 32 && row / (8 * cpt) <= 512 && 4 * row <= 64 * 1024) {
     switch (cpt * 100 + tph) {
-      case 101: return launch_tma<ACT, 1, 1>(p, stream);
-      case 201: return launch_tma<ACT, 2, 1>(p, stream);
-      case 401: return launch_tma<ACT, 4, 1>(p, stream);
-      case 402: return launch_tma<ACT, 4, 2>(p, stream);
-      case 404: return launch_tma<ACT, 4, 4>(p, stream);
-      case 408: return launch_tma<ACT, 4, 8>(p, stream);
-      case 416: return launch_tma<ACT, 4, 16>(p, stream);
-      case 432: return launch_tma<ACT, 4, 32>(p, stream);
+      case 101: return launch_tma<MODE, ACT, 1, 1>(p, stream);
+      case 201: return launch_tma<MODE, ACT, 2, 1>(p, stream);
+      case 401: return launch_tma<MODE, ACT, 4, 1>(p, stream);
+      case 402: return launch_tma<MODE, ACT, 4, 2>(p, stream);
+      case 404: return launch_tma<MODE, ACT, 4, 4>(p, stream);
+      case 408: return launch_tma<MODE, ACT, 4, 8>(p, stream);
+      case 416: return launch_tma<MODE, ACT, 4, 16>(p, stream);
+      case 432: return launch_tma<MODE, ACT, 4, 32>(p, stream);
       default: break;
     }
   }
-  return launch_generic<ACT>(p, stream);
+  return launch_generic<MODE, ACT>(p, stream);
+}
+
+template <int MODE>
+cudaError_t dispatch_act(const GatedParams& p, cudaStream_t stream) {
+  return p.act == kActSilu ? dispatch<MODE, kActSilu>(p, stream)
+                           : dispatch<MODE, kActSigmoid>(p, stream);
 }
 
 }  // namespace
 
 cudaError_t launch_gated(const GatedParams& p, cudaStream_t stream) {
-  return p.act == kActSilu ? dispatch<kActSilu>(p, stream) : dispatch<kActSigmoid>(p, stream);
+  switch (p.mode) {
+    case kModeNormQuant: return dispatch_act<kModeNormQuant>(p, stream);
+    case kModeGateQuant: return dispatch_act<kModeGateQuant>(p, stream);
+    case kModeQuant: return dispatch<kModeQuant, kActSigmoid>(p, stream);
+    case kModeNormOnly: return dispatch_act<kModeNormOnly>(p, stream);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 }  // namespace fp8n

@@ -8,7 +8,14 @@
 
 namespace fp8n {
 
+// Modes of the per-token kernels: (A) fused, and its steps on their own.
+constexpr int kModeNormQuant = 0;  // gated per-head RMSNorm, then per-token FP8
+constexpr int kModeGateQuant = 1;  // y = bf16(x * bf16(act(gate))), then per-token FP8
+constexpr int kModeQuant = 2;      // per-token FP8 of the bf16 row x
+constexpr int kModeNormOnly = 3;   // gated per-head RMSNorm to bf16 y
+
 struct GatedParams {
+  int mode;
   const uint16_t* x;
   int64_t x_stride;
   const uint16_t* gate;
@@ -21,6 +28,8 @@ struct GatedParams {
   uint8_t* out;
   int64_t out_stride;
   float* scale;
+  uint16_t* y_out;  // kModeNormOnly: bf16 [T, H*D]
+  int64_t y_stride;
   uint32_t* status;
 };
 
@@ -41,6 +50,7 @@ struct MxParams {
   int64_t q_scale_stride;
   uint16_t* kv_out;
   int64_t kv_out_stride;
+  int q_prenorm;  // q is already normalised: MX-quantise it as given (no q_weight)
   uint32_t* status;
 };
 
@@ -59,12 +69,31 @@ struct StaticParams {
   uint32_t* status;
 };
 
+// Dynamic per-head quantisation: the tensors of StaticParams with descale
+// outputs instead of inputs (StaticTensor::descale is written), and a
+// workspace of 3*H words that holds the per-head maxima between the passes.
+struct DynamicParams {
+  StaticParams s;
+  float* descale_out[3];
+  uint32_t* amax_bits;  // [3*H], overwritten
+};
+
+// Running per-head max |x| of one tensor: amax[h] = max(amax[h], max |x[:, h, :]|).
+struct AmaxParams {
+  const uint16_t* x;
+  int64_t tok_stride, head_stride, T;
+  int H, Dh;
+  float* amax;
+};
+
 // Number of streaming multiprocessors of the current device (cached per device).
 int sm_count();
 
 cudaError_t launch_gated(const GatedParams& p, cudaStream_t stream);
 cudaError_t launch_mx(const MxParams& p, cudaStream_t stream);
 cudaError_t launch_static(const StaticParams& p, cudaStream_t stream);
+cudaError_t launch_dynamic(const DynamicParams& p, cudaStream_t stream);
+cudaError_t launch_head_amax(const AmaxParams& p, cudaStream_t stream);
 cudaError_t launch_gate_act(const uint16_t* g, int64_t n, int act, uint16_t* out,
                             cudaStream_t stream);
 

@@ -13,6 +13,10 @@
 // of squares, then normalise + quantise).  An MX block is four consecutive
 // chunks, i.e. four neighbouring lanes of one step, so its amax takes two
 // xor-shuffles.  Rows longer than eight steps are read twice instead.
+//
+// The same kernels run the two steps of (B) on their own: with no q columns,
+// the row RMSNorm to bf16 (the kv path); with q_prenorm set, the MX
+// quantisation of an already normalised bf16 q.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -54,6 +58,29 @@ __device__ __forceinline__ int mx_exponent(uint32_t A) {
   return e < -127 ? -127 : e;  // E <= 127, so e <= 119
 }
 
+// ms = RN32(S / n) of one row from its double-float sum of squares S
+// (reduced over the warp, so every lane holds it and the flag is the same on
+// every lane), and whether S may not decide that rounding (then
+// row_ms_exact settles it).
+__device__ __forceinline__ float row_ms(df S, int n, bool n_pow2, int steps, bool* unsure) {
+  const float nf = (float)n;
+  const float ms = mean_from_sum(S, nf, 1.0f / nf, n_pow2);
+  *unsure = ms_uncertain(S, nf, ms, __fmaf_rn(S.h, sumsq_rel_err(4 * steps, 6), nf * 0x1p-149f));
+  return ms;
+}
+
+// The exact ms of a row whose double-float sum could not decide it: the
+// row's chunks (lane l holds chunks l, l + 32, ...) summed in double-double
+// over the warp.  Called by all lanes of the warp together.
+static __device__ __noinline__ float row_ms_exact(const uint4* row, int n, float ms, int lane) {
+  const int ch = n / 8;
+  const int cnt = lane < ch ? (ch - lane + 31) / 32 : 0;
+  dd Sd = sumsq_dd(row + lane, 32, cnt);
+#pragma unroll
+  for (int s = 16; s >= 1; s >>= 1) Sd = dd_add(Sd, shfl_xor_dd(Sd, s));
+  return ms_resolve(Sd, (float)n, ms);
+}
+
 // QS / KS: 512-byte steps of the q / kv row held in registers between the two
 // passes (0: the row is read again in the second pass).
 template <int QS, int KS>
@@ -65,13 +92,14 @@ __global__ void __launch_bounds__(kWarps * 32, (QS + KS >= 8) ? 2 : 3) rmsnorm_m
   const int qch = p.Nq / 8, kch = p.Nkv / 8;
   const int qsteps = (qch + 31) / 32, ksteps = (kch + 31) / 32;
   const bool q_pow2 = (p.Nq & (p.Nq - 1)) == 0, k_pow2 = (p.Nkv & (p.Nkv - 1)) == 0;
+  const bool q_norm = qch > 0 && !p.q_prenorm;
 
   for (int64_t m = gwarp; m < p.M; m += nwarps) {
     const uint16_t* qrow = p.q + m * p.q_stride;
     const uint16_t* krow = p.kv + m * p.kv_stride;
     constexpr int QR = QS > 0 ? QS : 1, KR = KS > 0 ? KS : 1;
     uint4 qr[QR], kr[KR];
-    kahan2 aq, ak;
+    sumsq2 aq, ak;
     if (RESIDENT) {
 #pragma unroll
       for (int j = 0; j < QR; ++j) {
@@ -85,11 +113,13 @@ __global__ void __launch_bounds__(kWarps * 32, (QS + KS >= 8) ? 2 : 3) rmsnorm_m
         kr[j] = make_uint4(0, 0, 0, 0);
         if (c < kch) kr[j] = *reinterpret_cast<const uint4*>(krow + 8 * c);
       }
+      if (!p.q_prenorm) {
 #pragma unroll
-      for (int j = 0; j < QR; ++j) {
-        const uint32_t* qw = &qr[j].x;
+        for (int j = 0; j < QR; ++j) {
+          const uint32_t* qw = &qr[j].x;
 #pragma unroll
-        for (int k = 0; k < 4; ++k) aq.add_sq(qw[k]);
+          for (int k = 0; k < 4; ++k) aq.add_sq(qw[k]);
+        }
       }
 #pragma unroll
       for (int j = 0; j < KR; ++j) {
@@ -98,7 +128,7 @@ __global__ void __launch_bounds__(kWarps * 32, (QS + KS >= 8) ? 2 : 3) rmsnorm_m
         for (int k = 0; k < 4; ++k) ak.add_sq(kw[k]);
       }
     } else {
-      for (int c = lane; c < qch; c += 32) {
+      for (int c = lane; c < (p.q_prenorm ? 0 : qch); c += 32) {
         const uint4 v = *reinterpret_cast<const uint4*>(qrow + 8 * c);
         const uint32_t* w = &v.x;
 #pragma unroll
@@ -117,10 +147,13 @@ __global__ void __launch_bounds__(kWarps * 32, (QS + KS >= 8) ? 2 : 3) rmsnorm_m
       Sq = df_add(Sq, shfl_xor_df(Sq, s));
       Sk = df_add(Sk, shfl_xor_df(Sk, s));
     }
-    const f2_t rq =
-        splat2(rms_factor(mean_from_sum(Sq, (float)p.Nq, 1.0f / (float)p.Nq, q_pow2), p.eps));
-    const f2_t rk = splat2(
-        kch ? rms_factor(mean_from_sum(Sk, (float)p.Nkv, 1.0f / (float)p.Nkv, k_pow2), p.eps) : 0.0f);
+    bool uq = false, uk = false;
+    float msq = q_norm ? row_ms(Sq, p.Nq, q_pow2, qsteps, &uq) : 0.0f;
+    float msk = kch ? row_ms(Sk, p.Nkv, k_pow2, ksteps, &uk) : 0.0f;
+    if (uq) msq = row_ms_exact(reinterpret_cast<const uint4*>(qrow), p.Nq, msq, lane);  // rare
+    if (uk) msk = row_ms_exact(reinterpret_cast<const uint4*>(krow), p.Nkv, msk, lane);
+    const f2_t rq = splat2(q_norm ? rms_factor(msq, p.eps) : 0.0f);
+    const f2_t rk = splat2(kch ? rms_factor(msk, p.eps) : 0.0f);
 
     uint8_t* qo = p.q_out + m * p.q_out_stride;
     uint8_t* so = p.q_scale + m * p.q_scale_stride;
@@ -129,10 +162,14 @@ __global__ void __launch_bounds__(kWarps * 32, (QS + KS >= 8) ? 2 : 3) rmsnorm_m
     // the block shuffles; lanes past the row end carry zeros)
     auto q_step = [&](int j, const uint4& xv) {
       const int c = 32 * j + lane;
-      uint4 wv = make_uint4(0, 0, 0, 0);
-      if (c < qch) wv = *reinterpret_cast<const uint4*>(p.q_weight + 8 * c);
       uint32_t y[4];
-      norm_chunk(xv, wv, rq, y);
+      if (p.q_prenorm) {
+        y[0] = xv.x, y[1] = xv.y, y[2] = xv.z, y[3] = xv.w;
+      } else {
+        uint4 wv = make_uint4(0, 0, 0, 0);
+        if (c < qch) wv = *reinterpret_cast<const uint4*>(p.q_weight + 8 * c);
+        norm_chunk(xv, wv, rq, y);
+      }
       uint32_t am = absmax_bf16x2(absmax_bf16x2(y[0], y[1]), absmax_bf16x2(y[2], y[3]));
       am = absmax_bf16x2(am, __shfl_xor_sync(0xFFFFFFFFu, am, 1));
       am = absmax_bf16x2(am, __shfl_xor_sync(0xFFFFFFFFu, am, 2));
@@ -160,27 +197,30 @@ __global__ void __launch_bounds__(kWarps * 32, (QS + KS >= 8) ? 2 : 3) rmsnorm_m
       const uint4 wv = *reinterpret_cast<const uint4*>(p.kv_weight + 8 * c);
       *reinterpret_cast<uint4*>(ko + 8 * c) = norm_chunk4(xv, wv, rk);
     };
-    if (RESIDENT) {
+    auto run_row = [&]() {
+      if (RESIDENT) {
 #pragma unroll
-      for (int j = 0; j < QR; ++j)
-        if (j < qsteps) q_step(j, qr[j]);
+        for (int j = 0; j < QR; ++j)
+          if (j < qsteps) q_step(j, qr[j]);
 #pragma unroll
-      for (int j = 0; j < KR; ++j)
-        if (j < ksteps) kv_step(j, kr[j]);
-    } else {
-      for (int j = 0; j < qsteps; ++j) {
-        const int c = 32 * j + lane;
-        uint4 xv = make_uint4(0, 0, 0, 0);
-        if (c < qch) xv = *reinterpret_cast<const uint4*>(qrow + 8 * c);
-        q_step(j, xv);
+        for (int j = 0; j < KR; ++j)
+          if (j < ksteps) kv_step(j, kr[j]);
+      } else {
+        for (int j = 0; j < qsteps; ++j) {
+          const int c = 32 * j + lane;
+          uint4 xv = make_uint4(0, 0, 0, 0);
+          if (c < qch) xv = *reinterpret_cast<const uint4*>(qrow + 8 * c);
+          q_step(j, xv);
+        }
+        for (int j = 0; j < ksteps; ++j) {
+          const int c = 32 * j + lane;
+          uint4 xv = make_uint4(0, 0, 0, 0);
+          if (c < kch) xv = *reinterpret_cast<const uint4*>(krow + 8 * c);
+          kv_step(j, xv);
+        }
       }
-      for (int j = 0; j < ksteps; ++j) {
-        const int c = 32 * j + lane;
-        uint4 xv = make_uint4(0, 0, 0, 0);
-        if (c < kch) xv = *reinterpret_cast<const uint4*>(krow + 8 * c);
-        kv_step(j, xv);
-      }
-    }
+    };
+    run_row();
   }
 }
 
@@ -248,9 +288,12 @@ __global__ void __launch_bounds__(kStagedMaxWarps * 32) rmsnorm_mx_tma(const MxP
   const uint4* wk = wq + qch;
   uint8_t* slots = smem + kStagedHeader + slot_bytes + (size_t)warp * kSlots * slot_bytes;
   const bool q_pow2 = (p.Nq & (p.Nq - 1)) == 0, k_pow2 = (p.Nkv & (p.Nkv - 1)) == 0;
-  for (int i = threadIdx.x; i < qch + kch; i += blockDim.x)
-    const_cast<uint4*>(wq)[i] = i < qch ? reinterpret_cast<const uint4*>(p.q_weight)[i]
-                                        : reinterpret_cast<const uint4*>(p.kv_weight)[i - qch];
+  for (int i = threadIdx.x; i < qch + kch; i += blockDim.x) {
+    if (i >= qch)
+      const_cast<uint4*>(wq)[i] = reinterpret_cast<const uint4*>(p.kv_weight)[i - qch];
+    else if (!p.q_prenorm)
+      const_cast<uint4*>(wq)[i] = reinterpret_cast<const uint4*>(p.q_weight)[i];
+  }
   __syncthreads();
 
   if (lane == 0) {
@@ -262,7 +305,7 @@ __global__ void __launch_bounds__(kStagedMaxWarps * 32) rmsnorm_mx_tma(const MxP
     const uint32_t bar = smem_u32(&bars[s]);
     const uint32_t dst = smem_u32(slots + (size_t)s * slot_bytes);
     mbar_expect_tx(bar, slot_bytes);
-    bulk_g2s(dst, p.q + m * p.q_stride, qbytes, bar);
+    if (qbytes) bulk_g2s(dst, p.q + m * p.q_stride, qbytes, bar);
     if (kbytes) bulk_g2s(dst + qbytes, p.kv + m * p.kv_stride, kbytes, bar);
   };
   if (lane == 0)
@@ -279,8 +322,8 @@ __global__ void __launch_bounds__(kStagedMaxWarps * 32) rmsnorm_mx_tma(const MxP
     if (__any_sync(0xFFFFFFFFu, timeout)) break;
     const uint4* sq = reinterpret_cast<const uint4*>(slots + (size_t)s * slot_bytes);
     const uint4* sk = reinterpret_cast<const uint4*>(slots + (size_t)s * slot_bytes + qbytes);
-    kahan2 aq, ak;
-    for (int c = lane; c < qch; c += 32) {
+    sumsq2 aq, ak;
+    for (int c = lane; c < (p.q_prenorm ? 0 : qch); c += 32) {
       const uint4 v = sq[c];
       const uint32_t* w = &v.x;
 #pragma unroll
@@ -298,41 +341,52 @@ __global__ void __launch_bounds__(kStagedMaxWarps * 32) rmsnorm_mx_tma(const MxP
       Sq = df_add(Sq, shfl_xor_df(Sq, o));
       Sk = df_add(Sk, shfl_xor_df(Sk, o));
     }
-    const f2_t rq =
-        splat2(rms_factor(mean_from_sum(Sq, (float)p.Nq, 1.0f / (float)p.Nq, q_pow2), p.eps));
-    const f2_t rk = splat2(
-        kch ? rms_factor(mean_from_sum(Sk, (float)p.Nkv, 1.0f / (float)p.Nkv, k_pow2), p.eps) : 0.0f);
+    const int qsteps = (qch + 31) / 32;
+    const bool q_norm = qch > 0 && !p.q_prenorm;
+    bool uq = false, uk = false;
+    float msq = q_norm ? row_ms(Sq, p.Nq, q_pow2, qsteps, &uq) : 0.0f;
+    float msk = kch ? row_ms(Sk, p.Nkv, k_pow2, (kch + 31) / 32, &uk) : 0.0f;
+    if (uq) msq = row_ms_exact(sq, p.Nq, msq, lane);  // rare; uq, uk are warp-uniform
+    if (uk) msk = row_ms_exact(sk, p.Nkv, msk, lane);
+    const f2_t rq = splat2(q_norm ? rms_factor(msq, p.eps) : 0.0f);
+    const f2_t rk = splat2(kch ? rms_factor(msk, p.eps) : 0.0f);
     uint8_t* qo = p.q_out + m * p.q_out_stride;
     uint8_t* so = p.q_scale + m * p.q_scale_stride;
     uint16_t* ko = p.kv_out + m * p.kv_out_stride;
-    const int qsteps = (qch + 31) / 32;
-    for (int j = 0; j < qsteps; ++j) {  // warp-uniform: every lane takes part in the shuffles
-      const int c = 32 * j + lane;
-      uint4 xv = make_uint4(0, 0, 0, 0), wv = xv;
-      if (c < qch) {
-        xv = sq[c];
-        wv = wq[c];
-      }
-      uint32_t y[4];
-      norm_chunk(xv, wv, rq, y);
-      const uint32_t code = mx_code(block_amax_bits(y));
-      if (c < qch) {
-        if ((lane & 3) == 0) so[c >> 2] = (uint8_t)code;
-        uint2 o;
-        if (code == 0xFFu) {
-          o = make_uint2(0x7F7F7F7Fu, 0x7F7F7F7Fu);
-        } else {
-          const f2_t sc = splat2(pow2i(127 - (int)code));  // 2^-e, exact scaling
-          uint32_t b[4];
-#pragma unroll
-          for (int k = 0; k < 4; ++k) b[k] = f2_to_e4m3x2(mul2(bf2_to_f2(y[k]), sc));
-          o = make_uint2(b[0] | (b[1] << 16), b[2] | (b[3] << 16));
+    auto run_row = [&]() {
+      for (int j = 0; j < qsteps; ++j) {  // warp-uniform: every lane takes part in the shuffles
+        const int c = 32 * j + lane;
+        uint4 xv = make_uint4(0, 0, 0, 0), wv = xv;
+        if (c < qch) {
+          xv = sq[c];
+          if (!p.q_prenorm) wv = wq[c];
         }
-        *reinterpret_cast<uint2*>(qo + 8 * c) = o;
+        uint32_t y[4];
+        if (p.q_prenorm) {
+          y[0] = xv.x, y[1] = xv.y, y[2] = xv.z, y[3] = xv.w;
+        } else {
+          norm_chunk(xv, wv, rq, y);
+        }
+        const uint32_t code = mx_code(block_amax_bits(y));
+        if (c < qch) {
+          if ((lane & 3) == 0) so[c >> 2] = (uint8_t)code;
+          uint2 o;
+          if (code == 0xFFu) {
+            o = make_uint2(0x7F7F7F7Fu, 0x7F7F7F7Fu);
+          } else {
+            const f2_t sc = splat2(pow2i(127 - (int)code));  // 2^-e, exact scaling
+            uint32_t b[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) b[k] = f2_to_e4m3x2(mul2(bf2_to_f2(y[k]), sc));
+            o = make_uint2(b[0] | (b[1] << 16), b[2] | (b[3] << 16));
+          }
+          *reinterpret_cast<uint2*>(qo + 8 * c) = o;
+        }
       }
-    }
-    for (int c = lane; c < kch; c += 32)
-      *reinterpret_cast<uint4*>(ko + 8 * c) = norm_chunk4(sk[c], wk[c], rk);
+      for (int c = lane; c < kch; c += 32)
+        *reinterpret_cast<uint4*>(ko + 8 * c) = norm_chunk4(sk[c], wk[c], rk);
+    };
+    run_row();
     __syncwarp();  // every lane is done with slot s
     if (lane == 0) {
       const int64_t mn = m + kSlots * nwarps;

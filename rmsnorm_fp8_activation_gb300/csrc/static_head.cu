@@ -48,17 +48,38 @@ struct Flat {
   FastDiv heads;      // H
   uint32_t n[3];      // chunks per tensor
   int H;
+  int ntensors;       // tensors walked (the amax pass of a single tensor: 1)
   uint32_t* status;
+  int* amax_bits;     // dynamic variant: [3*H] per-head max |x| as float bits
+  float* dout[3];     // dynamic variant: descale outputs
 };
 
 // Per-head constants: the descale d, -RN(1/d), the bf16 pair +-T with
 // T = RU_bf16(512 d) (|x| above T saturates to 448 anyway, and clamping it
-// keeps x * (1/d) finite), and whether d is finite and positive.
+// keeps x * (1/d) finite), and which quotient path d takes: kFast for
+// 2^-92 <= d <= 2^126, where 1/d is a normal binary32 and the FMA residual
+// cannot underflow for any quotient that reaches a nonzero code
+// (|x/d| >= 2^-11); kZero for the zero descale of an all-zero head in the
+// dynamic variant (signed zero codes); kExact, the plain IEEE division, for
+// every other d.
+constexpr uint32_t kFast = 0, kExact = 1, kZero = 2;
 struct HeadConst {
   float d, nrd;
   uint32_t clamp2;
-  uint32_t ok;
+  uint32_t path;
 };
+
+__device__ __forceinline__ HeadConst head_const(float d, bool dynamic) {
+  HeadConst hc;
+  hc.d = d;
+  hc.path = (d >= 0x1p-92f && d <= 0x1p126f) ? kFast : (dynamic && d == 0.0f) ? kZero : kExact;
+  hc.nrd = -__frcp_rn(d);
+  uint32_t b = __float_as_uint(__fmul_rn(d, 512.0f));
+  if (b & 0xFFFFu) b += 0x10000u;                            // round up to bf16
+  const uint32_t t = hc.path == kFast ? (b >> 16) : 0x7F80u;  // inf: no clamp
+  hc.clamp2 = t | (t << 16);
+  return hc;
+}
 
 __device__ __forceinline__ uint32_t bf16x2_min_nan(uint32_t a, uint32_t b) {
   uint32_t d;
@@ -75,7 +96,8 @@ __device__ __forceinline__ uint32_t bf16x2_max_nan(uint32_t a, uint32_t b) {
 // FMA correction, arranged on -x (q0 = (-x)(-1/d), e = q0 d - x, q = q0 - e/d)
 // so that signed zeros keep their sign.
 __device__ __forceinline__ uint32_t quot_pair(uint32_t x, const HeadConst& hc) {
-  if (!hc.ok) {  // any other descale: the plain IEEE quotient
+  if (hc.path != kFast) {
+    if (hc.path == kZero) return (x >> 8 & 0x80u) | (x >> 16 & 0x8000u);  // the signs of x
     return e4m3x2(__fdiv_rn(bf16_lo(x), hc.d), __fdiv_rn(bf16_hi(x), hc.d));
   }
   x = bf16x2_max_nan(bf16x2_min_nan(x, hc.clamp2), hc.clamp2 | 0x80008000u);
@@ -86,22 +108,23 @@ __device__ __forceinline__ uint32_t quot_pair(uint32_t x, const HeadConst& hc) {
   return f2_to_e4m3x2(fma2(e, nrd, q0));
 }
 
+// DYN: the descales are RN32(amax / 448) of the per-head maxima that the
+// amax pass left in f.amax_bits (float bits); block 0 also writes them out.
+template <bool DYN>
 __global__ void __launch_bounds__(kThreads) static_head_kernel(const Flat f) {
   __shared__ HeadConst hcs[3 * kMaxHeads];
   const int nh = 3 * f.H;
   bool any_bad = false;
   for (int i = threadIdx.x; i < nh; i += blockDim.x) {
-    const float d = f.t[i / f.H].descale[i % f.H];
-    HeadConst hc;
-    hc.d = d;
-    hc.ok = (d > 0.0f) && (d <= 3.402823466e38f);  // finite and positive
-    hc.nrd = -__frcp_rn(d);
-    uint32_t b = __float_as_uint(__fmul_rn(d, 512.0f));
-    if (b & 0xFFFFu) b += 0x10000u;                   // round up to bf16
-    const uint32_t t = hc.ok ? (b >> 16) : 0x7F80u;   // inf: no clamp
-    hc.clamp2 = t | (t << 16);
-    hcs[i] = hc;
-    any_bad |= !hc.ok;
+    float d;
+    if (DYN) {
+      d = __fdiv_rn(__int_as_float(f.amax_bits[i]), 448.0f);
+      if (blockIdx.x == 0) f.dout[i / f.H][i % f.H] = d;
+    } else {
+      d = f.t[i / f.H].descale[i % f.H];
+      any_bad |= !((d > 0.0f) && (d <= 3.402823466e38f));  // not finite and positive
+    }
+    hcs[i] = head_const(d, DYN);
   }
   if (any_bad && blockIdx.x == 0 && f.status) atomicOr(f.status, kStatusBadDescale);
   __syncthreads();
@@ -144,10 +167,72 @@ __global__ void __launch_bounds__(kThreads) static_head_kernel(const Flat f) {
   }
 }
 
-}  // namespace
+// Per-head max |x| (the amax pass of the dynamic variant, and the running
+// maxima of calibration).  bf16 magnitudes order like their bit patterns with
+// the sign cleared, NaN above infinity above every finite value, so the max
+// is an unsigned 16-bit max on packed pairs.  When the grid-stride S is a
+// multiple of every tensor's chunks per token, each thread's chunks all sit
+// in one head and its running max is folded into shared memory once per
+// tensor; otherwise (UNIFORM false) it is folded whenever the head changes.
+// Each block then takes its per-head maxima to f.amax_bits with one atomic
+// max each (as ints: non-negative float bits order like the values).
+template <bool UNIFORM>
+__global__ void __launch_bounds__(kThreads) head_amax_kernel(const Flat f) {
+  __shared__ int hmax[3 * kMaxHeads];
+  const int nh = f.ntensors * f.H;
+  for (int i = threadIdx.x; i < nh; i += blockDim.x) hmax[i] = 0;
+  __syncthreads();
+  const uint32_t stride = gridDim.x * blockDim.x;
+  const uint32_t first = blockIdx.x * blockDim.x + threadIdx.x;
+  auto head_of = [&](uint32_t c, const FastDiv& cpr) {
+    const uint32_t row = fdiv(c, cpr);
+    return row - fdiv(row, f.heads) * f.heads.d;
+  };
+  auto fold = [&](int* slot, uint32_t m2) {
+    const uint32_t m = max(m2 & 0xFFFFu, m2 >> 16);
+    if (m) atomicMax(slot, (int)(m << 16));
+  };
+#pragma unroll 1
+  for (int ti = 0; ti < f.ntensors; ++ti) {
+    const StaticTensor T = f.t[ti];
+    const FastDiv cpr = f.cpr[ti];
+    const uint32_t n = f.n[ti];
+    if (first >= n) continue;
+    int* hm = hmax + ti * f.H;
+    uint32_t cur = head_of(first, cpr), m2 = 0;
+    for (uint32_t base = first; base < n; base += stride * kUnroll) {
+      uint4 v[kUnroll];
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) {
+        const uint32_t c = base + u * stride;
+        v[u] = make_uint4(0, 0, 0, 0);
+        if (c < n) {
+          const uint32_t row = fdiv(c, cpr);
+          const uint32_t col = c - row * cpr.d;
+          const uint32_t tok = fdiv(row, f.heads);
+          const uint32_t h = row - tok * f.heads.d;
+          v[u] = __ldcs(reinterpret_cast<const uint4*>(T.x + (int64_t)tok * T.tok_stride +
+                                                       (int64_t)h * T.head_stride + 8 * col));
+          if (!UNIFORM && h != cur) {
+            fold(&hm[cur], m2);
+            cur = h;
+            m2 = 0;
+          }
+        }
+        const uint32_t a = __vmaxu2(v[u].x & 0x7FFF7FFFu, v[u].y & 0x7FFF7FFFu);
+        const uint32_t b = __vmaxu2(v[u].z & 0x7FFF7FFFu, v[u].w & 0x7FFF7FFFu);
+        m2 = __vmaxu2(m2, __vmaxu2(a, b));
+      }
+    }
+    fold(&hm[cur], m2);
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < nh; i += blockDim.x)
+    if (hmax[i]) atomicMax(&f.amax_bits[i], hmax[i]);
+}
 
-cudaError_t launch_static(const StaticParams& p, cudaStream_t stream) {
-  Flat f;
+Flat make_flat(const StaticParams& p, uint32_t* max_chunks) {
+  Flat f = {};
   uint32_t acc = 0;
   for (int i = 0; i < 3; ++i) {
     f.t[i] = p.t[i];
@@ -158,16 +243,102 @@ cudaError_t launch_static(const StaticParams& p, cudaStream_t stream) {
   }
   f.heads = make_fastdiv((uint32_t)p.H);
   f.H = p.H;
+  f.ntensors = 3;
   f.status = p.status;
+  *max_chunks = acc;
+  return f;
+}
+
+template <typename K>
+cudaError_t persistent_grid(K kern, uint32_t max_chunks, int* grid) {
   int per_sm = 0;
-  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, static_head_kernel, kThreads, 0);
+  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, 0);
   if (e != cudaSuccess) return e;
   if (per_sm < 1) per_sm = 1;
   const int64_t want = (int64_t)sm_count() * per_sm;
-  const int64_t need = ((int64_t)acc + kThreads * kUnroll - 1) / (kThreads * kUnroll);
-  const int grid = (int)(need < want ? need : want);
-  static_head_kernel<<<grid, kThreads, 0, stream>>>(f);
+  const int64_t need = ((int64_t)max_chunks + kThreads * kUnroll - 1) / (kThreads * kUnroll);
+  *grid = (int)(need < want ? need : want);
+  return cudaSuccess;
+}
+
+uint64_t gcd64(uint64_t a, uint64_t b) {
+  while (b) {
+    const uint64_t t = a % b;
+    a = b;
+    b = t;
+  }
+  return a;
+}
+
+// The amax pass over f.ntensors tensors into f.amax_bits.  The grid is a
+// multiple of the block count that makes the grid-stride a multiple of every
+// tensor's chunks per token (the uniform case), when that multiple fits in
+// the persistent grid.
+cudaError_t launch_amax_pass(const Flat& f, uint32_t max_chunks, cudaStream_t stream) {
+  int grid = 0;
+  cudaError_t e = persistent_grid(head_amax_kernel<true>, max_chunks, &grid);
+  if (e != cudaSuccess) return e;
+  uint64_t L = 1;
+  for (int i = 0; i < f.ntensors; ++i) {
+    const uint64_t C = (uint64_t)f.heads.d * f.cpr[i].d;  // chunks per token
+    L = L / gcd64(L, C) * C;
+    if (L > (1u << 30)) break;
+  }
+  const uint64_t unit = L / gcd64(L, kThreads);  // blocks per uniform step
+  int want = 0;
+  e = persistent_grid(head_amax_kernel<true>, 0xFFFFFFFFu, &want);
+  if (e != cudaSuccess) return e;
+  if (unit <= (uint64_t)want) {
+    const int g = (int)((uint64_t)want / unit * unit);
+    head_amax_kernel<true><<<g, kThreads, 0, stream>>>(f);
+  } else {
+    head_amax_kernel<false><<<grid, kThreads, 0, stream>>>(f);
+  }
   return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_static(const StaticParams& p, cudaStream_t stream) {
+  uint32_t chunks = 0;
+  const Flat f = make_flat(p, &chunks);
+  int grid = 0;
+  cudaError_t e = persistent_grid(static_head_kernel<false>, chunks, &grid);
+  if (e != cudaSuccess) return e;
+  static_head_kernel<false><<<grid, kThreads, 0, stream>>>(f);
+  return cudaGetLastError();
+}
+
+// Dynamic per-head quantisation: zero the maxima, the amax pass, then the
+// quantisation pass with descales RN32(amax / 448) (two launches, no waits).
+cudaError_t launch_dynamic(const DynamicParams& p, cudaStream_t stream) {
+  uint32_t chunks = 0;
+  Flat f = make_flat(p.s, &chunks);
+  f.amax_bits = reinterpret_cast<int*>(p.amax_bits);
+  for (int i = 0; i < 3; ++i) f.dout[i] = p.descale_out[i];
+  f.status = nullptr;
+  cudaError_t e = cudaMemsetAsync(p.amax_bits, 0, sizeof(uint32_t) * 3 * (size_t)p.s.H, stream);
+  if (e != cudaSuccess) return e;
+  e = launch_amax_pass(f, chunks, stream);
+  if (e != cudaSuccess) return e;
+  int grid = 0;
+  e = persistent_grid(static_head_kernel<true>, chunks, &grid);
+  if (e != cudaSuccess) return e;
+  static_head_kernel<true><<<grid, kThreads, 0, stream>>>(f);
+  return cudaGetLastError();
+}
+
+// Calibration: the running per-head maxima of one tensor, folded into amax.
+cudaError_t launch_head_amax(const AmaxParams& p, cudaStream_t stream) {
+  StaticParams s = {};
+  for (int i = 0; i < 3; ++i) s.t[i] = {p.x, p.tok_stride, p.head_stride, p.Dh, nullptr, nullptr};
+  s.T = p.T;
+  s.H = p.H;
+  uint32_t chunks = 0;
+  Flat f = make_flat(s, &chunks);
+  f.ntensors = 1;
+  f.amax_bits = reinterpret_cast<int*>(p.amax);
+  return launch_amax_pass(f, chunks, stream);
 }
 
 }  // namespace fp8n

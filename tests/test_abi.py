@@ -42,7 +42,7 @@ def test_status_strings(L):
     for code in range(7):
         s = L.fp8n_status_string(code).decode()
         assert s.startswith("FP8N_")
-    assert L.fp8n_version() == 0x000100
+    assert L.fp8n_version() == 0x000200
 
 
 # Validation paths return before touching the device.
@@ -132,3 +132,58 @@ def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
     monkeypatch.setattr(B, "LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError, match="no fallback"):
         B.lib()
+
+
+def test_step_entry_points_validation(L):
+    # per-token quantisation of bf16 rows
+    assert L.fp8n_quant_token(P16, 4096, 0, 4096, P16, 4096, P16, None, None) == OK
+    assert L.fp8n_quant_token(P16, 4096, 3, 12, P16, 4096, P16, None, None) == UNSUPPORTED
+    assert L.fp8n_quant_token(P16, 4096, 3, 16392, P16, 16392, P16, None, None) == UNSUPPORTED
+    assert L.fp8n_quant_token(P16, 132, 3, 128, P16, 128, P16, None, None) == MISALIGNED
+    assert L.fp8n_quant_token(P16, 64, 3, 128, P16, 128, P16, None, None) == SHAPE
+    assert L.fp8n_quant_token(None, 128, 3, 128, P16, 128, P16, None, None) == NULL
+    assert L.fp8n_quant_token(P16, 128, 3, 128, P16, 128, None, None, None) == NULL
+    assert L.fp8n_quant_token(P16, 128, 3, 128, P16, 132, P16, None, None) == MISALIGNED
+    # gate product + quantisation
+    g = L.fp8n_gated_quant_token
+    assert g(P16, 128, P16, 128, 3, 128, 2, P16, 128, P16, None, None) == UNSUPPORTED
+    assert g(P16, 128, None, 128, 3, 128, 0, P16, 128, P16, None, None) == NULL
+    assert g(P16, 128, P16 + 8, 128, 3, 128, 1, P16, 128, P16, None, None) == MISALIGNED
+    assert g(P16, 128, P16, 120, 3, 128, 1, P16, 128, P16, None, None) == SHAPE
+    # gated norm to bf16
+    n = L.fp8n_gated_rmsnorm_bf16
+    assert n(P16, 512, P16, 512, P16, 0, 4, 128, 1e-6, 0, P16, 512, None, None) == OK
+    assert n(P16, 512, P16, 512, P16, 2, 4, 128, 1e-6, 0, P16, 500, None, None) == SHAPE
+    assert n(P16, 512, P16, 512, P16, 2, 4, 128, 1e-6, 0, None, 512, None, None) == NULL
+    assert n(P16, 512, P16, 512, P16, 2, 4, 128, float("inf"), 0, P16, 512, None, None) == UNSUPPORTED
+    assert n(P16, 512, P16, 512, P16, 2, 4, 12, 1e-6, 0, P16, 512, None, None) == UNSUPPORTED
+    # row RMSNorm to bf16 and MX quantisation
+    assert L.fp8n_rmsnorm_bf16(P16, 512, P16, 0, 512, 1e-6, P16, 512, None, None) == OK
+    assert L.fp8n_rmsnorm_bf16(P16, 512, P16, 4, 500, 1e-6, P16, 512, None, None) == UNSUPPORTED
+    assert L.fp8n_rmsnorm_bf16(P16, 512, None, 4, 512, 1e-6, P16, 512, None, None) == NULL
+    assert L.fp8n_rmsnorm_bf16(P16, 512, P16, 4, 512, 1e-6, P16 + 4, 512, None, None) == MISALIGNED
+    assert L.fp8n_quant_mx(P16, 512, 0, 512, P16, 512, P16, 16, None, None) == OK
+    assert L.fp8n_quant_mx(P16, 512, 4, 520, P16, 520, P16, 17, None, None) == UNSUPPORTED
+    assert L.fp8n_quant_mx(P16, 512, 4, 512, P16, 512, P16, 15, None, None) == SHAPE
+    assert L.fp8n_quant_mx(P16, 512, 4, 512, P16, 512, None, 16, None, None) == NULL
+
+
+def test_dynamic_and_amax_validation(L):
+    def dyn(**kw):
+        a = dict(q=P16, k=P16, v=P16, qts=2304, qhs=192, vts=1536, vhs=128, T=10, H=12, Dqk=192,
+                 Dv=128, ws=P16, qd=P16, kd=P16, vd=P16, qo=P16, ko=P16, vo=P16)
+        a.update(kw)
+        return L.fp8n_dynamic_head_quant(a["q"], a["k"], a["v"], a["qts"], a["qhs"], a["vts"],
+                                         a["vhs"], a["T"], a["H"], a["Dqk"], a["Dv"], a["ws"],
+                                         a["qd"], a["kd"], a["vd"], a["qo"], a["ko"], a["vo"], None)
+    assert dyn(T=0) == OK
+    assert dyn(H=257) == UNSUPPORTED
+    assert dyn(ws=None) == NULL
+    assert dyn(kd=None) == NULL
+    assert dyn(ws=P16 + 2) == MISALIGNED
+    assert dyn(vhs=120) == SHAPE
+    assert L.fp8n_head_amax(P16, 2304, 192, 0, 12, 192, P16, None) == OK
+    assert L.fp8n_head_amax(P16, 2304, 192, 10, 12, 196, P16, None) == UNSUPPORTED
+    assert L.fp8n_head_amax(P16, 2304, 100, 10, 12, 192, P16, None) == SHAPE
+    assert L.fp8n_head_amax(P16, 2304, 192, 10, 12, 192, None, None) == NULL
+    assert L.fp8n_head_amax(P16 + 8, 2304, 192, 10, 12, 192, P16, None) == MISALIGNED

@@ -266,8 +266,9 @@ def test_static_small_varlen():
 
 
 def test_static_division_all_bf16_numerators():
-    """every bf16 value divided by 36 descales (random, and ones such as 3 and 7
-    whose reciprocal is inexact), against the oracle's IEEE quotient."""
+    """every bf16 value divided by 36 descales (random, ones such as 3 and 7
+    whose reciprocal is inexact, and the extremes of the binary32 range),
+    against the oracle's IEEE quotient."""
     x = np.arange(65536, dtype=np.uint16)
     x = np.where((x & 0x7F80) == 0x7F80, 0x3F80, x).astype(np.uint16)   # finite only
     H, D = 12, 128
@@ -276,6 +277,9 @@ def test_static_division_all_bf16_numerators():
     rng = np.random.default_rng(9)
     ds = {k: (10.0 ** rng.uniform(-6, 3, H)).astype(np.float32) for k in ("q", "k", "v")}
     ds["k"][:6] = np.array([3, 7, 1.0 / 3, 11, 0.1, 1e-5], np.float32)
+    # both ends of the reciprocal path (2^-92 .. 2^126) and beyond it
+    ds["v"][:8] = np.array([2.0 ** -100, 2.0 ** -92, 1.5 * 2.0 ** -93, 2.0 ** 125, 2.0 ** 126,
+                            1.5 * 2.0 ** 126, 1e-40, np.finfo(np.float32).max], np.float32)
     xs = {"q": q, "k": q, "v": q}
     assert check_static(xs, ds) == 0
 

@@ -1,0 +1,364 @@
+"""GPU parity of the standalone steps against the oracle, and the fused
+operations against their unfused pipelines (bit for bit, both on the GPU).
+
+  * per-token FP8 of bf16 rows, with and without the gate product in front;
+  * the gated RMSNorm of (A) to bf16;
+  * the row RMSNorm to bf16 and the MXFP8 quantisation that make up (B);
+  * the dynamic per-head Q/K/V quantisation and the calibration maxima.
+
+Tolerances are those of the path (tests/parity.py): bf16 outputs, E8M0 codes,
+descales and the per-head codes bit-exact; per-token codes within the one-code
+budget and scales within 1e-6 relative.  The fused-versus-unfused checks are
+exact: every rounding of the fused kernels is the one of the separate steps.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+import parity as P
+import synth
+
+pytestmark = pytest.mark.gpu
+
+B = None
+W = synth.workloads()
+
+
+@pytest.fixture(scope="module", autouse=True)
+def lib():
+    global B
+    if not torch.cuda.is_available():
+        pytest.fail("CUDA device required for -m gpu tests")
+    from rmsnorm_fp8_activation_gb300 import build
+    build.build()
+    import rmsnorm_fp8_activation_gb300 as mod
+    B = mod
+    mod.lib()
+    yield
+
+
+def dev16(a: np.ndarray) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).cuda().view(torch.bfloat16)
+
+
+def host16(t: torch.Tensor) -> np.ndarray:
+    return t.view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def rows(stream: int, T: int, N: int, sigma=1.0, outlier_p=0.01, outlier_scale=60.0):
+    return synth.bf16_normal(11, stream, T * N, sigma=sigma, outlier_p=outlier_p,
+                             outlier_scale=outlier_scale).reshape(T, N)
+
+
+def special_rows(N: int) -> np.ndarray:
+    """Rows that exercise the quantiser's edge cases: all +0, all -0 mixed with
+    +0, tiny values whose scale falls below 2^-60 and below 2^-126, values at
+    the top of the bf16 range, one dominant element, and an exact E4M3 tie
+    under a scale between 2^-126 and 2^-60 (the residual of the reciprocal
+    quotient would underflow there without the 2^64 rescale)."""
+    r = np.zeros((9, N), np.uint16)
+    r[1, ::2] = 0x8000                                   # signed zeros
+    r[2] = rows(90, 1, N, sigma=1e-22, outlier_p=0)[0]   # scale ~ 2^-80
+    r[3] = rows(91, 1, N, sigma=1e-36, outlier_p=0)[0]   # scale below 2^-126
+    r[4, :] = 0x0001                                     # smallest subnormal
+    r[4, 1::3] = 0x8003
+    r[5] = rows(92, 1, N, sigma=1e37, outlier_p=0)[0]    # near the top of bf16
+    r[6] = rows(93, 1, N)[0]
+    r[6, N // 2] = 0x4B00                                # one dominant element
+    r[7] = rows(94, 1, N, sigma=1e-16, outlier_p=0)[0]   # scale ~ 2^-60 (tiny path edge)
+    r[8, 0] = 0x07C4                                     # amax 1.53125 * 2^-112: s = 7 * 2^-123
+    r[8, 1] = 0x005B                                     # y / s = 13/1024, an E4M3 tie
+    r[8, 2] = 0x805B
+    return r
+
+
+# ---------------------------------------------------------------------------
+# per-token quantisation of bf16 rows
+# ---------------------------------------------------------------------------
+
+def check_quant_token(y):
+    oc, os_ = B.fp8n_quant_token(dev16(y))
+    torch.cuda.synchronize()
+    wc, ws = O.quant_token(y)
+    got_c, got_s = oc.cpu().numpy(), os_.cpu().numpy()
+    P.compare_scales(got_s, ws)
+    P.compare_codes(got_c, wc)
+    P.compare_dequant(got_c, got_s, wc, ws)
+    return got_c, wc
+
+
+@pytest.mark.parametrize("T,N", [(1, 8), (5, 40), (37, 128), (300, 1536), (61, 4096),
+                                 (17, 8192), (9, 16384), (23, 12296), (13, 16376)])
+def test_quant_token_shapes(T, N):
+    check_quant_token(rows(N, T, N))
+
+
+@pytest.mark.parametrize("N", [128, 4104])
+def test_quant_token_special_rows(N):
+    got, want = check_quant_token(special_rows(N))
+    assert np.array_equal(got, want)
+
+
+def test_quant_token_strided_rows():
+    T, N = 70, 1024
+    y = rows(5, T, N)
+    buf = np.zeros((T, N + 40), np.uint16)
+    buf[:, :N] = y
+    oc, os_ = B.fp8n_quant_token(dev16(buf)[:, :N])
+    torch.cuda.synchronize()
+    wc, ws = O.quant_token(y)
+    P.compare_scales(os_.cpu().numpy(), ws)
+    P.compare_codes(oc.cpu().numpy(), wc)
+
+
+# ---------------------------------------------------------------------------
+# gate product + per-token quantisation
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("T,N", [(3, 8), (40, 96), (129, 2048), (7, 16384), (2600, 16384)])
+@pytest.mark.parametrize("act", [O.ACT_SIGMOID, O.ACT_SILU])
+def test_gated_quant_token(T, N, act):
+    """(2600, 16384) is long enough for the kernel's gate table."""
+    x = rows(200 + N, T, N)
+    g = rows(300 + N, T, N, sigma=3.0)
+    oc, os_ = B.fp8n_gated_quant_token(dev16(x), dev16(g), act)
+    torch.cuda.synchronize()
+    _, wc, ws = O.gated_quant_token(x, g, act)
+    got_c, got_s = oc.cpu().numpy(), os_.cpu().numpy()
+    P.compare_scales(got_s, ws)
+    P.compare_codes(got_c, wc)
+    P.compare_dequant(got_c, got_s, wc, ws)
+
+
+# ---------------------------------------------------------------------------
+# gated RMSNorm to bf16, and (A) against its unfused pipeline
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("T,H,D", [(1, 1, 8), (9, 3, 40), (56, 12, 128), (33, 4, 256),
+                                   (5, 2, 8192), (700, 32, 128)])
+@pytest.mark.parametrize("act", [O.ACT_SIGMOID, O.ACT_SILU])
+def test_gated_rmsnorm_bf16(T, H, D, act):
+    x = rows(400 + D, T, H * D).reshape(T, H, D)
+    g = rows(500 + D, T, H * D, sigma=2.0).reshape(T, H, D)
+    w = synth.bf16_normal(11, 600 + D, D, sigma=0.1, mean=1.0)
+    y = B.fp8n_gated_rmsnorm_bf16(dev16(x), dev16(g), dev16(w), 1e-6, act)
+    torch.cuda.synchronize()
+    assert np.array_equal(host16(y), O.gated_rmsnorm_bf16(x, g, w, 1e-6, act))
+
+
+@pytest.mark.parametrize("name,T", [("gated_small", 56), ("gated_silu", 4096),
+                                    ("gated_large", 8192)])
+def test_gated_fused_equals_unfused(name, T):
+    """quant_token(gated_rmsnorm_bf16(x)) == gated_rmsnorm_quant_token(x), codes
+    and scales bit for bit (8192 tokens of the large workload take the gate
+    table in both kernels)."""
+    w = W[name]
+    x, g, wt = dev16(w.x(0, T)), dev16(w.gate(0, T)), dev16(w.weight())
+    c1, s1 = B.fp8n_gated_rmsnorm_quant_token(x, g, wt, w.eps, w.act)
+    y = B.fp8n_gated_rmsnorm_bf16(x, g, wt, w.eps, w.act)
+    c2, s2 = B.fp8n_quant_token(y)
+    torch.cuda.synchronize()
+    assert torch.equal(c1, c2)
+    assert torch.equal(s1.view(torch.int32), s2.view(torch.int32))
+    if name == "gated_small":
+        assert np.array_equal(host16(y), O.gated_rmsnorm_bf16(w.x(), w.gate(), w.weight(),
+                                                              w.eps, w.act))
+
+
+# ---------------------------------------------------------------------------
+# (B): row RMSNorm to bf16, MX quantisation, fused against unfused
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("M,N", [(1, 8), (7, 512), (100, 1536), (3, 2048), (5, 4096),
+                                 (2, 16384), (9, 3064)])
+def test_rmsnorm_bf16(M, N):
+    x = rows(700 + N, M, N, sigma=1.4)
+    w = synth.bf16_normal(11, 800 + N, N, sigma=0.1, mean=1.0)
+    y = B.fp8n_rmsnorm_bf16(dev16(x), dev16(w), 1e-6)
+    torch.cuda.synchronize()
+    assert np.array_equal(host16(y), O.rmsnorm_bf16(x, w, 1e-6))
+
+
+@pytest.mark.parametrize("M,N", [(1, 32), (7, 96), (100, 1536), (3, 4096), (2, 16384)])
+def test_quant_mx(M, N):
+    y = rows(900 + N, M, N, sigma=3.0, outlier_p=0.02, outlier_scale=1e4)
+    y[0, :32] = 0                                        # a zero block
+    y[-1, -32:] = 0x0001                                 # a subnormal block
+    oc, osc = B.fp8n_quant_mx(dev16(y))
+    torch.cuda.synchronize()
+    wc, ws = O.quant_mx(y)
+    assert np.array_equal(osc.cpu().numpy(), ws)         # E8M0: bit-exact
+    assert np.array_equal(oc.cpu().numpy(), wc)          # exact power-of-two scaling
+
+
+@pytest.mark.parametrize("M", [777, 8192])
+def test_mx_fused_equals_unfused(M):
+    """The fused producer equals RMSNorm-to-bf16 followed by MX quantisation,
+    bit for bit, on the q/kv workload (the property its source states)."""
+    w = W["qkv_mx"]
+    q, kv = dev16(w.q(0, M)), dev16(w.kv(0, M))
+    wq, wkv = dev16(w.q_weight()), dev16(w.kv_weight())
+    qo, qs, ko = B.fp8n_rmsnorm_quant_mx(q, wq, kv, wkv, w.eps)
+    yq = B.fp8n_rmsnorm_bf16(q, wq, w.eps)
+    qo2, qs2 = B.fp8n_quant_mx(yq)
+    ko2 = B.fp8n_rmsnorm_bf16(kv, wkv, w.eps)
+    torch.cuda.synchronize()
+    assert torch.equal(qs, qs2)
+    assert torch.equal(qo, qo2)
+    assert torch.equal(ko.view(torch.int16), ko2.view(torch.int16))
+
+
+# ---------------------------------------------------------------------------
+# dynamic per-head quantisation and calibration maxima
+# ---------------------------------------------------------------------------
+
+def check_dynamic(xs, pad_tok=0):
+    def put(a):
+        if not pad_tok:
+            return dev16(a)
+        T, H, D = a.shape
+        buf = np.zeros((T, H * D + pad_tok), np.uint16)
+        buf[:, :H * D] = a.reshape(T, -1)
+        return dev16(buf)[:, :H * D].view(T, H, D)
+    ds, outs = B.fp8n_dynamic_head_quant(put(xs["q"]), put(xs["k"]), put(xs["v"]))
+    torch.cuda.synchronize()
+    for i, k in enumerate(("q", "k", "v")):
+        wd, wc = O.dynamic_head_quant(xs[k])
+        gd = ds[i].cpu().numpy()
+        assert np.array_equal(gd.view(np.uint32), wd.view(np.uint32)), k
+        assert np.array_equal(outs[i].cpu().numpy(), wc), k
+
+
+def test_dynamic_small_varlen():
+    sw = synth.StaticHeadWorkload("t", lengths=np.array([3, 130, 1, 77]))
+    xs = {k: sw.tensor(k) for k in ("q", "k", "v")}
+    check_dynamic(xs)
+    check_dynamic(xs, pad_tok=64)
+
+
+def test_dynamic_special_heads():
+    """A zero head (signed zeros), heads of tiny values whose descale falls
+    below 2^-92 and below 2^-126, and a head near the top of the bf16 range."""
+    sw = synth.StaticHeadWorkload("t", lengths=np.array([40, 9]))
+    xs = {k: sw.tensor(k).copy() for k in ("q", "k", "v")}
+    T = sw.T
+    xs["q"][:, 0, :] = 0
+    xs["q"][::3, 0, ::5] = 0x8000
+    xs["q"][:, 1, :] = rows(60, T, 192, sigma=1e-27, outlier_p=0).reshape(T, 192)
+    xs["k"][:, 2, :] = rows(61, T, 192, sigma=1e-37, outlier_p=0).reshape(T, 192)
+    xs["k"][:, 3, :] = rows(62, T, 192, sigma=1e36, outlier_p=0).reshape(T, 192)
+    xs["v"][:, 4, :] = 0x0001
+    check_dynamic(xs)
+
+
+@pytest.mark.parametrize("H,Dqk,Dv", [(1, 8, 8), (5, 64, 24), (16, 128, 128), (3, 576, 512)])
+def test_dynamic_shapes(H, Dqk, Dv):
+    T = 257
+    xs = {"q": rows(70 + Dqk, T, H * Dqk).reshape(T, H, Dqk),
+          "k": rows(71 + Dqk, T, H * Dqk, sigma=3.0).reshape(T, H, Dqk),
+          "v": rows(72 + Dv, T, H * Dv, sigma=0.5).reshape(T, H, Dv)}
+    check_dynamic(xs)
+
+
+def test_dynamic_full_size_sampled():
+    """The full packed workload: descales from all of Q, K, V exactly; codes on
+    sampled tokens (sequence starts and random ones)."""
+    sw = W["static_head"]
+    xs = {k: sw.tensor(k) for k in ("q", "k", "v")}
+    ds, outs = B.fp8n_dynamic_head_quant(dev16(xs["q"]), dev16(xs["k"]), dev16(xs["v"]))
+    torch.cuda.synchronize()
+    toks = np.unique(np.concatenate([[0, sw.T - 1], sw.cu_seqlens()[1:-1],
+                                     np.random.default_rng(8).integers(0, sw.T, 200)]))
+    idx = torch.from_numpy(toks).cuda()
+    for i, k in enumerate(("q", "k", "v")):
+        # descale = RN32(amax / 448) with amax the oracle's maxima over all tokens
+        want_d = O.dynamic_head_quant(head_tensor(O.head_amax(xs[k])))[0]
+        gd = ds[i].cpu().numpy()
+        assert np.array_equal(gd.view(np.uint32), want_d.view(np.uint32)), k
+        want_codes = O.static_head_quant(xs[k][toks], want_d)
+        assert np.array_equal(outs[i][idx].cpu().numpy(), want_codes), k
+
+
+def head_tensor(amax: np.ndarray) -> np.ndarray:
+    """A one-token tensor [1, H, 8] whose head h holds amax[h] (a bf16 value,
+    as every maximum of bf16 data is), so that the oracle's dynamic quantiser
+    returns RN32(amax / 448) for each head."""
+    bits = (amax.astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    assert np.array_equal((bits.astype(np.uint32) << 16).view(np.float32), amax)
+    t = np.zeros((1, amax.size, 8), np.uint16)
+    t[0, :, 0] = bits
+    return t
+
+
+def test_head_amax_running():
+    """Two calls fold into the same maxima (calibration over two batches)."""
+    sw = W["static_head"]
+    a = sw.tensor("q", 0, 3000)
+    b = sw.tensor("q", 5000, 1000).copy()
+    b[7, 3, 11] = 0x7FC0                                 # a NaN in head 3
+    amax = B.fp8n_head_amax(dev16(a))
+    B.fp8n_head_amax(dev16(b), amax)
+    torch.cuda.synchronize()
+    want = O.head_amax(b, O.head_amax(a))
+    got = amax.cpu().numpy()
+    nan = np.isnan(want)
+    assert nan[3] and np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], want[~nan])
+
+
+@pytest.mark.parametrize("H,Dh,tok_pad", [(1, 8, 0), (12, 192, 0), (12, 128, 40), (7, 520, 8)])
+def test_head_amax_shapes(H, Dh, tok_pad):
+    T = 333
+    x = rows(80 + Dh, T, H * Dh, sigma=2.0).reshape(T, H, Dh)
+    if tok_pad:
+        buf = np.zeros((T, H * Dh + tok_pad), np.uint16)
+        buf[:, :H * Dh] = x.reshape(T, -1)
+        xt = dev16(buf)[:, :H * Dh].view(T, H, Dh)
+    else:
+        xt = dev16(x)
+    got = B.fp8n_head_amax(xt).cpu().numpy()
+    assert np.array_equal(got, O.head_amax(x))
+
+
+# ---------------------------------------------------------------------------
+# mean squares on rounding boundaries
+# ---------------------------------------------------------------------------
+
+# Heads whose exact mean square lies on a binary32 rounding boundary (an even
+# tie), each followed by the same head plus one value of 2^-40, whose square
+# (2^-80) breaks the tie upwards; found by exhaustive search on the host.  The
+# kernels' double-float sums cannot see the 2^-80, flag the head as
+# undecided and settle it in double-double: the bf16 outputs of the first
+# four elements differ between the two heads of each pair.
+TIE_HEADS = [
+    [0x3F93, 0x3F98, 0x3D37, 0x3D37, 0, 0, 0, 0],
+    [0x3F93, 0x3F98, 0x3D37, 0x3D37, 0x2B80, 0, 0, 0],
+    [0x3FA2, 0x3F88, 0x3D6B, 0x3D6B, 0, 0, 0, 0],
+    [0x3FA2, 0x3F88, 0x3D6B, 0x3D6B, 0x2B80, 0, 0, 0],
+    [0x3FA7, 0x3F84, 0x3B30, 0x3B30, 0, 0, 0, 0],
+    [0x3FA7, 0x3F84, 0x3B30, 0x3B30, 0x2B80, 0, 0, 0],
+]
+
+
+@pytest.mark.parametrize("D", [8, 128])
+def test_mean_square_ties(D):
+    x = np.zeros((len(TIE_HEADS), D), np.uint16)
+    x[:, :8] = np.array(TIE_HEADS, np.uint16)
+    w = np.full(D, 0x3F80, np.uint16)
+    y = host16(B.fp8n_rmsnorm_bf16(dev16(x), dev16(w), 0.0))
+    want = O.rmsnorm_bf16(x, w, 0.0)
+    assert np.array_equal(y, want)
+    assert all((want[i, :4] != want[i + 1, :4]).any() for i in range(0, len(TIE_HEADS), 2))
+    # the same heads through the gated norm (gate 100: sigmoid rounds to 1)
+    g = np.full(x.shape, 0x42C8, np.uint16)
+    for H in (1, 2):
+        xt = x.reshape(-1, H, D)
+        gt = g.reshape(-1, H, D)
+        yg = host16(B.fp8n_gated_rmsnorm_bf16(dev16(xt), dev16(gt), dev16(w), 0.0, O.ACT_SIGMOID))
+        assert np.array_equal(yg, O.gated_rmsnorm_bf16(xt, gt, w, 0.0, O.ACT_SIGMOID))
+    # and as the kv rows of the fused (B) producer
+    q = np.zeros((len(TIE_HEADS), 32), np.uint16)
+    _, _, ko = B.fp8n_rmsnorm_quant_mx(dev16(q), dev16(np.full(32, 0x3F80, np.uint16)), dev16(x),
+                                       dev16(w), 0.0)
+    assert np.array_equal(host16(ko), want)
