@@ -259,6 +259,34 @@ fp8n_status fp8n_dynamic_head_quant(const void* q, const void* k, const void* v,
                                     void* q_out, void* k_out, void* v_out, fp8n_stream_t stream);
 
 /*
+ * fp8n_dynamic_head_quant without a workspace argument: the same computation
+ * and outputs, for callers that cannot allocate device memory, such as code
+ * embedded in a host application that owns all device memory through its
+ * own fixed pool (allocating outside it breaks the host's memory accounting),
+ * or code on a latency-critical path where cudaMalloc would synchronise the
+ * device.  This entry point has no counterpart in the paper.
+ *
+ * The per-head maxima are kept in a static device array of the library
+ * (3 * 256 words, 3 KB, held by every GPU that loads the library until the
+ * process exits).  The first call on each device looks up that array's
+ * device address (cudaGetSymbolAddress) and caches it; make that first call
+ * before any stream capture.  The call allocates nothing and zeroes the
+ * array on `stream` before using it.  All calls share the one array: two
+ * calls whose work overlaps on the GPU (different streams, or the same array
+ * in use by an earlier call not yet finished on another stream) race and
+ * may produce wrong descales; order them on one stream or with events.
+ * Limits as fp8n_dynamic_head_quant; H above 256 is rejected with
+ * FP8N_ERR_UNSUPPORTED.
+ */
+fp8n_status fp8n_dynamic_head_quant_noalloc(const void* q, const void* k, const void* v,
+                                            int64_t qk_tok_stride, int64_t qk_head_stride,
+                                            int64_t v_tok_stride, int64_t v_head_stride,
+                                            int64_t T, int32_t H, int32_t Dqk, int32_t Dv,
+                                            float* q_descale, float* k_descale, float* v_descale,
+                                            void* q_out, void* k_out, void* v_out,
+                                            fp8n_stream_t stream);
+
+/*
  * Calibration: running per-head maxima of one packed tensor,
  *   amax[h] = max(amax[h], max_{t,d} |x[t,h,d]|),
  * as collected after warm-up to build (C)'s descales.  Source: "[ROCm][MLA]

@@ -74,6 +74,9 @@ def lib() -> ctypes.CDLL:
         L.fp8n_dynamic_head_quant.argtypes = [
             P, P, P, i64, i64, i64, i64, i64, i32, i32, i32, P, P, P, P, P, P, P, P]
         L.fp8n_head_amax.argtypes = [P, i64, i64, i64, i32, i32, P, P]
+        L.fp8n_dynamic_head_quant_noalloc.argtypes = [
+            P, P, P, i64, i64, i64, i64, i64, i32, i32, i32, P, P, P, P, P, P, P]
+        L.fp8n_dynamic_head_quant_noalloc.restype = ctypes.c_int
         for name in ("fp8n_gated_rmsnorm_bf16", "fp8n_quant_token", "fp8n_gated_quant_token",
                      "fp8n_rmsnorm_bf16", "fp8n_quant_mx", "fp8n_dynamic_head_quant",
                      "fp8n_head_amax"):
@@ -342,3 +345,28 @@ def fp8n_head_amax(x, amax=None, stream=None):
     _check("fp8n_head_amax", lib().fp8n_head_amax(
         _ptr(x), x.stride(0), x.stride(1), T, H, Dh, _ptr(amax), _stream(stream)))
     return amax
+
+
+def fp8n_dynamic_head_quant_noalloc(q, k, v, descales=None, q_out=None, k_out=None, v_out=None,
+                                    stream=None):
+    """fp8n_dynamic_head_quant with the library's static scratch instead of a
+    workspace (for callers that cannot allocate device memory; the outputs
+    must still be passed or are allocated here by torch).  Calls whose work
+    overlaps on the GPU race on the shared scratch."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _need(t, n, _BF16, 3)
+    T, H, Dqk = q.shape
+    Dv = v.shape[2]
+    if k.shape != q.shape or v.shape[:2] != (T, H) or k.stride() != q.stride():
+        raise ValueError("q and k must share shape and strides; v must match [T, H]")
+    dev = q.device
+    if descales is None:
+        descales = tuple(torch.empty((H,), dtype=torch.float32, device=dev) for _ in range(3))
+    outs = []
+    for o, d in ((q_out, Dqk), (k_out, Dqk), (v_out, Dv)):
+        outs.append(o if o is not None else torch.empty((T, H, d), dtype=torch.uint8, device=dev))
+    _check("fp8n_dynamic_head_quant_noalloc", lib().fp8n_dynamic_head_quant_noalloc(
+        _ptr(q), _ptr(k), _ptr(v), q.stride(0), q.stride(1), v.stride(0), v.stride(1), T, H, Dqk,
+        Dv, _ptr(descales[0]), _ptr(descales[1]), _ptr(descales[2]), _ptr(outs[0]), _ptr(outs[1]),
+        _ptr(outs[2]), _stream(stream)))
+    return tuple(descales), tuple(outs)

@@ -2,6 +2,7 @@
 // caller's stream (see include/fp8norm.h for the contract of each call).
 #include <cmath>
 #include <cstdint>
+#include <mutex>
 #include <vector>
 
 #include "fp8norm.h"
@@ -356,6 +357,72 @@ fp8n_status fp8n_dynamic_head_quant(const void* q, const void* k, const void* v,
   p.descale_out[1] = k_descale;
   p.descale_out[2] = v_descale;
   p.amax_bits = workspace;
+  return cuda_status(fp8n::launch_dynamic(p, (cudaStream_t)stream));
+}
+
+}  // extern "C"
+
+// ---- dynamic per-head quantisation without a caller workspace --------------
+//
+// The per-head maxima of fp8n_dynamic_head_quant_noalloc live in this
+// file-scope device array instead of a caller buffer.  Every GPU that loads
+// the library holds it (3 * 256 words, 3 KB) until the process exits.  Host
+// code may not pass the array's name to a kernel (on the host it is only a
+// stand-in for the device symbol): its device address is looked up once per
+// device with cudaGetSymbolAddress and cached.
+namespace {
+
+constexpr int kNoAllocMaxHeads = 256;
+constexpr int kNoAllocMaxDevices = 64;
+static __device__ __align__(256) uint32_t g_dynamic_scratch[3 * kNoAllocMaxHeads];
+
+std::mutex g_scratch_mutex;
+uint32_t* g_scratch_address[kNoAllocMaxDevices] = {};
+
+// Device address of g_dynamic_scratch on the current device (looked up on
+// the first call for that device).
+fp8n_status noalloc_scratch(uint32_t** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_status(e);
+  if (dev < 0 || dev >= kNoAllocMaxDevices) return FP8N_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_scratch_mutex);
+  if (!g_scratch_address[dev]) {
+    void* ptr = nullptr;
+    e = cudaGetSymbolAddress(&ptr, g_dynamic_scratch);
+    if (e != cudaSuccess) return cuda_status(e);
+    g_scratch_address[dev] = static_cast<uint32_t*>(ptr);
+  }
+  *out = g_scratch_address[dev];
+  return FP8N_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+fp8n_status fp8n_dynamic_head_quant_noalloc(const void* q, const void* k, const void* v,
+                                            int64_t qk_tok_stride, int64_t qk_head_stride,
+                                            int64_t v_tok_stride, int64_t v_head_stride,
+                                            int64_t T, int32_t H, int32_t Dqk, int32_t Dv,
+                                            float* q_descale, float* k_descale, float* v_descale,
+                                            void* q_out, void* k_out, void* v_out,
+                                            fp8n_stream_t stream) {
+  if (H > kNoAllocMaxHeads) return FP8N_ERR_UNSUPPORTED;  // beyond the static scratch
+  fp8n::DynamicParams p = {};
+  fp8n_status s = check_qkv(q, k, v, qk_tok_stride, qk_head_stride, v_tok_stride, v_head_stride,
+                            T, H, Dqk, Dv, q_out, k_out, v_out, &p.s);
+  if (s != FP8N_OK || T == 0) return s;
+  if (!q_descale || !k_descale || !v_descale) return FP8N_ERR_NULL;
+  if (misaligned4(q_descale) || misaligned4(k_descale) || misaligned4(v_descale))
+    return FP8N_ERR_MISALIGNED;
+  uint32_t* scratch = nullptr;
+  s = noalloc_scratch(&scratch);
+  if (s != FP8N_OK) return s;
+  p.descale_out[0] = q_descale;
+  p.descale_out[1] = k_descale;
+  p.descale_out[2] = v_descale;
+  p.amax_bits = scratch;  // zeroed on the stream by the launcher before use
   return cuda_status(fp8n::launch_dynamic(p, (cudaStream_t)stream));
 }
 
