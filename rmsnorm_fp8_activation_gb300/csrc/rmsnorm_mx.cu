@@ -69,12 +69,22 @@ __device__ __forceinline__ float row_ms(df S, int n, bool n_pow2, int steps, boo
   return ms;
 }
 
-// The exact ms of a row whose double-float sum could not decide it: the
-// row's chunks (lane l holds chunks l, l + 32, ...) summed in double-double
-// over the warp.  Called by all lanes of the warp together.
-static __device__ __noinline__ float row_ms_exact(const uint4* row, int n, float ms, int lane) {
+// The exact ms of a row whose double-float sum S could not decide it: when
+// S is itself exact (sum_is_exact over the row's elements; lane l holds
+// chunks l, l + 32, ...) in binary32, else from the chunks summed in
+// double-double over the warp.  Called by all lanes of the warp together.
+static __device__ __noinline__ float row_ms_exact(const uint4* row, int n, df S, int steps, float ms,
+                                                  int lane) {
   const int ch = n / 8;
   const int cnt = lane < ch ? (ch - lane + 31) / 32 : 0;
+  uint32_t emin = 255u;
+  for (int i = 0; i < cnt; ++i) {
+    const uint4 v = row[lane + 32 * i];
+    emin = emin_pair(emin_pair(emin_pair(emin_pair(emin, v.x), v.y), v.z), v.w);
+  }
+#pragma unroll
+  for (int s = 16; s >= 1; s >>= 1) emin = min(emin, __shfl_xor_sync(0xFFFFFFFFu, emin, s));
+  if (sum_is_exact(emin, S.h, 4 * steps)) return ms_resolve_exact(S, (float)n, ms);
   dd Sd = sumsq_dd(row + lane, 32, cnt);
 #pragma unroll
   for (int s = 16; s >= 1; s >>= 1) Sd = dd_add(Sd, shfl_xor_dd(Sd, s));
@@ -150,8 +160,8 @@ __global__ void __launch_bounds__(kWarps * 32, (QS + KS >= 8) ? 2 : 3) rmsnorm_m
     bool uq = false, uk = false;
     float msq = q_norm ? row_ms(Sq, p.Nq, q_pow2, qsteps, &uq) : 0.0f;
     float msk = kch ? row_ms(Sk, p.Nkv, k_pow2, ksteps, &uk) : 0.0f;
-    if (uq) msq = row_ms_exact(reinterpret_cast<const uint4*>(qrow), p.Nq, msq, lane);  // rare
-    if (uk) msk = row_ms_exact(reinterpret_cast<const uint4*>(krow), p.Nkv, msk, lane);
+    if (uq) msq = row_ms_exact(reinterpret_cast<const uint4*>(qrow), p.Nq, Sq, qsteps, msq, lane);  // rare
+    if (uk) msk = row_ms_exact(reinterpret_cast<const uint4*>(krow), p.Nkv, Sk, ksteps, msk, lane);
     const f2_t rq = splat2(q_norm ? rms_factor(msq, p.eps) : 0.0f);
     const f2_t rk = splat2(kch ? rms_factor(msk, p.eps) : 0.0f);
 
@@ -346,8 +356,8 @@ __global__ void __launch_bounds__(kStagedMaxWarps * 32) rmsnorm_mx_tma(const MxP
     bool uq = false, uk = false;
     float msq = q_norm ? row_ms(Sq, p.Nq, q_pow2, qsteps, &uq) : 0.0f;
     float msk = kch ? row_ms(Sk, p.Nkv, k_pow2, (kch + 31) / 32, &uk) : 0.0f;
-    if (uq) msq = row_ms_exact(sq, p.Nq, msq, lane);  // rare; uq, uk are warp-uniform
-    if (uk) msk = row_ms_exact(sk, p.Nkv, msk, lane);
+    if (uq) msq = row_ms_exact(sq, p.Nq, Sq, qsteps, msq, lane);  // rare; uq, uk are warp-uniform
+    if (uk) msk = row_ms_exact(sk, p.Nkv, Sk, (kch + 31) / 32, msk, lane);
     const f2_t rq = splat2(q_norm ? rms_factor(msq, p.eps) : 0.0f);
     const f2_t rk = splat2(kch ? rms_factor(msk, p.eps) : 0.0f);
     uint8_t* qo = p.q_out + m * p.q_out_stride;

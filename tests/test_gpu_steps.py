@@ -357,8 +357,27 @@ def test_mean_square_ties(D):
         gt = g.reshape(-1, H, D)
         yg = host16(B.fp8n_gated_rmsnorm_bf16(dev16(xt), dev16(gt), dev16(w), 0.0, O.ACT_SIGMOID))
         assert np.array_equal(yg, O.gated_rmsnorm_bf16(xt, gt, w, 0.0, O.ACT_SIGMOID))
+        # the fused quantisation settles these heads in its fix-up pass
+        c, s = B.fp8n_gated_rmsnorm_quant_token(dev16(xt), dev16(gt), dev16(w), 0.0, O.ACT_SIGMOID)
+        wc, ws = O.gated_rmsnorm_quant_token(xt, gt, w, 0.0, O.ACT_SIGMOID)
+        assert np.array_equal(c.cpu().numpy(), wc)
+        assert np.array_equal(s.cpu().numpy().view(np.uint32), ws.view(np.uint32))
     # and as the kv rows of the fused (B) producer
     q = np.zeros((len(TIE_HEADS), 32), np.uint16)
     _, _, ko = B.fp8n_rmsnorm_quant_mx(dev16(q), dev16(np.full(32, 0x3F80, np.uint16)), dev16(x),
                                        dev16(w), 0.0)
     assert np.array_equal(host16(ko), want)
+
+
+def test_zero_eps_with_idle_lanes():
+    """eps = 0 with rows shorter than the kernel's thread block (idle lanes see
+    zero heads, whose own factor would be 1/sqrt(0)): the idle lanes must not
+    reach the token's amax."""
+    for (T, H, D) in ((5, 1, 8), (7, 3, 128), (4, 12, 128)):
+        x = rows(1000 + D + H, T, H * D).reshape(T, H, D)
+        g = rows(1100 + D + H, T, H * D, sigma=2.0).reshape(T, H, D)
+        w = synth.bf16_normal(11, 1200 + D, D, sigma=0.1, mean=1.0)
+        c, s = B.fp8n_gated_rmsnorm_quant_token(dev16(x), dev16(g), dev16(w), 0.0, O.ACT_SILU)
+        wc, ws = O.gated_rmsnorm_quant_token(x, g, w, 0.0, O.ACT_SILU)
+        P.compare_scales(s.cpu().numpy(), ws)
+        P.compare_codes(c.cpu().numpy(), wc)

@@ -216,10 +216,27 @@ def _kahan(values):
 def _device_head(xs, head, lane_sum=None):
     """Double-float S of one head of 128 values as the staged kernel forms it
     for D = 128 (four threads of four 8-element chunks): thread j = 4 head + i
-    reads its chunks in the rotated order (c + j / 2) % 4, keeps two packed
-    lanes (even / odd elements), and the four threads meet in an xor
-    butterfly."""
+    reads chunk (c + j / 2) % 4 at step c into chain c % 2, each chain with
+    two packed lanes (even / odd elements); the chains meet in one df_add and
+    the four threads in an xor butterfly."""
     lane_sum = lane_sum or _sumsq2
+    parts = []
+    for i in range(4):
+        j = 4 * head + i
+        chunks = [xs[32 * i + 8 * c: 32 * i + 8 * c + 8] for c in range(4)]
+        order = [chunks[(c + j // 2) % 4] for c in range(4)]
+        chains = []
+        for ch in (order[0] + order[2], order[1] + order[3]):
+            e, o = lane_sum(ch[0::2]), lane_sum(ch[1::2])
+            chains.append(_df_add(_fast_two_sum(*e), _fast_two_sum(*o)))
+        parts.append(_df_add(chains[0], chains[1]))
+    for m in (1, 2):
+        parts = [_df_add(parts[i], parts[i ^ m]) for i in range(4)]
+    return parts[0]
+
+
+def _single_chain_head(xs, head, lane_sum):
+    """The earlier layout: one chain per thread over the four rotated chunks."""
     parts = []
     for i in range(4):
         j = 4 * head + i
@@ -246,15 +263,15 @@ def _ms_uncertain(S, n, ms, err):
 
 
 def test_mean_square_is_decided_or_flagged():
-    """For heads of 128 values (4 threads of 32, the staged kernel's layout),
+    """For heads of 128 values (the staged kernel's layout and bound),
     including heavy outliers and the head that exposed an ordinary Kahan sum,
     the binary32 mean square from the device double-float either equals
     RN32(S / 128) of the exact S or is flagged for the double-double path, by
     either of the two flag tests the kernels use."""
     import numpy as np
     import synth
-    k, adds = 16, 3
-    rel = Fraction((k * k + 4 * adds + 16)) * Fraction(2) ** -47
+    k, adds = 8, 5
+    rel = Fraction((k * k + 4 * adds + 16)) * Fraction(2) ** -48
     rng = np.random.default_rng(4)
     heads = []
     x = synth.bf16_normal(11, 528, 700 * 32 * 128, outlier_p=0.01,
@@ -264,7 +281,9 @@ def test_mean_square_is_decided_or_flagged():
     y = synth.bf16_normal(12, 9, 40 * 128, sigma=1.0, outlier_p=0.2, outlier_scale=1e4)
     heads += list(y.reshape(40, 128))
     heads.append(np.full(128, 0x3FC0, np.uint16))              # constant head: exact S
-    flagged = 0
+    z = synth.bf16_normal(13, 9, 60 * 128, sigma=0.3, mean=1.5).reshape(60, 128)
+    heads += list(z)                                           # narrow range: exact sums, ties
+    flagged = certified = 0
     for n_head, hx in enumerate(heads):
         xs = [X.bf16_to_frac(int(b)) for b in hx]
         S_exact = sum((v * v for v in xs), Fraction(0))
@@ -276,11 +295,67 @@ def test_mean_square_is_decided_or_flagged():
         probe = S[0] != 0 and rn32(S[0] + rn32(S[1] + err)) != rn32(S[0] + rn32(S[1] - err))
         # the other kernels' test: the residual's distance to a boundary
         near = _ms_uncertain(S, 128, ms, err)
-        if probe or near:
+        # the exactness certificate (smallest nonzero exponent against S)
+        emin = min(((int(b) >> 7) & 0xFF) for b in hx if int(b) & 0x7FFF)
+        E = X.floor_log2(S[0]) + 127
+        if emin >= 60 and 2 * emin >= E + 95 + 2:
+            certified += 1
+            assert S[0] + S[1] == S_exact
+        elif probe or near:
             flagged += 1
         if not probe or not near:
             assert ms == rn32(S_exact / 128)
-        if n_head == 0:   # the ordinary Kahan sum misses this head by one ulp
-            K = _device_head(xs, head, _kahan)
+        if n_head == 0:   # an ordinary Kahan sum (one chain per thread) misses it by one ulp
+            K = _single_chain_head(xs, head, _kahan)
             assert rn32(rn32(K[0] + K[1]) / 128) != ms
-    assert flagged <= 3
+    assert flagged <= 3 and certified >= 50
+
+
+def _resolve_exact(S, n, ms):
+    """The kernels' binary32 resolve of RN32(S / n) for an exact double-float S."""
+    h, l = S
+    for _ in range(4):
+        r1 = rn32(h - ms * n)                       # FMA, exact
+        up = X.f32_bits_to_frac(_bits(ms) + 1)
+        dn = X.f32_bits_to_frac(_bits(ms) - 1) if ms > 0 else Fraction(0)
+        hu = rn32(rn32(rn32(up - ms) / 2) * n)
+        hd = rn32(rn32(rn32(ms - dn) / 2) * n)
+        du = rn32(rn32(r1 - hu) + l)
+        dl = rn32(rn32(r1 + hd) + l)
+        odd = _bits(ms) & 1
+        if du > 0 or (du == 0 and odd):
+            ms = up
+        elif ms > 0 and (dl < 0 or (dl == 0 and odd)):
+            ms = dn
+        else:
+            break
+    return ms
+
+
+def _bits(v: Fraction) -> int:
+    return struct.unpack("<I", struct.pack("<f", float(v)))[0]
+
+
+def test_binary32_resolve_of_exact_sums():
+    """For exact double-float sums S (up to 48 significant bits, including
+    exact ties of S / n) and row lengths n that are not powers of two, the
+    binary32 resolve steps any start within two ulps to RN32(S / n)."""
+    import random
+    rng = random.Random(31)
+    for n in (1536, 40, 96, 120, 512, 16384):
+        for _ in range(300):
+            e = rng.randrange(-20, 40)
+            S = Fraction(rng.getrandbits(47) | (1 << 47), 1 << 47) * Fraction(2) ** e
+            if rng.random() < 0.3:                  # an exact tie of S / n
+                q = rn32(S / n)
+                ulp = Fraction(2) ** (X.floor_log2(q) - 23)
+                S = (q + ulp / 2) * n
+                if X.round_rne(S, 48, -1000) != S:
+                    continue
+            h = rn32(S)
+            l = rn32(S - h)
+            assert h + l == S
+            want = rn32(S / n)
+            for k in (-2, -1, 0, 1, 2):
+                start = X.f32_bits_to_frac(_bits(want) + k)
+                assert _resolve_exact((h, l), n, start) == want, (n, S, k)
