@@ -222,6 +222,60 @@ def reference_arm(args, rank: int, world: int) -> None:
 
 
 # ---------------------------------------------------------------------------
+# the fused operations against their unfused steps, and the dynamic per-head
+# quantisation (reported beside the step, not part of it)
+# ---------------------------------------------------------------------------
+
+def side_measurements(dev, d16, inp_c) -> dict:
+    """Median device time over 30 launches (L2 flushed before each) of: (A) at
+    the gated_silu size fused and as gated norm -> bf16 -> per-token quant;
+    (B) at the qkv_mx size fused and as RMSNorm -> bf16 -> MX quant plus the
+    kv RMSNorm; the dynamic per-head quantisation of the static_head
+    workload (max pass + quantise pass)."""
+    import torch
+    import synth
+    import rmsnorm_fp8_activation_gb300 as B
+    W = synth.workloads()
+    ws, wm = W["gated_silu"], W["qkv_mx"]
+    x, gt, w = d16(ws.x()), d16(ws.gate()), d16(ws.weight())
+    q, kv, wq, wkv = d16(wm.q()), d16(wm.kv()), d16(wm.q_weight()), d16(wm.kv_weight())
+    Q, K, V = d16(inp_c["q"]), d16(inp_c["k"]), d16(inp_c["v"])
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    def timed(fn, n=30):
+        fn()
+        ts = []
+        for _ in range(n):
+            flush.zero_()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            torch.cuda.synchronize()
+            ts.append(1e3 * e0.elapsed_time(e1))
+        return statistics.median(ts)
+
+    a_fused = timed(lambda: B.fp8n_gated_rmsnorm_quant_token(x, gt, w, ws.eps, ws.act))
+    a_unfused = timed(lambda: B.fp8n_quant_token(B.fp8n_gated_rmsnorm_bf16(x, gt, w, ws.eps, ws.act)))
+    b_fused = timed(lambda: B.fp8n_rmsnorm_quant_mx(q, wq, kv, wkv, wm.eps))
+    b_unfused = timed(lambda: (B.fp8n_quant_mx(B.fp8n_rmsnorm_bf16(q, wq, wm.eps)),
+                               B.fp8n_rmsnorm_bf16(kv, wkv, wm.eps)))
+    dyn = timed(lambda: B.fp8n_dynamic_head_quant(Q, K, V))
+    n_c = Q.numel() + K.numel() + V.numel()
+    return {
+        "gated_silu_fused_us": a_fused, "gated_silu_unfused_us": a_unfused,
+        "gated_silu_unfused_steps": "fp8n_gated_rmsnorm_bf16 -> fp8n_quant_token",
+        "qkv_mx_fused_us": b_fused, "qkv_mx_unfused_us": b_unfused,
+        "qkv_mx_unfused_steps": "fp8n_rmsnorm_bf16(q) -> fp8n_quant_mx; fp8n_rmsnorm_bf16(kv)",
+        "dynamic_head_quant_us": dyn,
+        "dynamic_head_quant_GB_s": 5 * n_c / (dyn * 1e-6) / 1e9,
+        "dynamic_head_quant_bytes": "2 B/element read twice, 1 B/element written",
+        "l2": "flushed (256 MB write) before each launch",
+    }
+
+
+# ---------------------------------------------------------------------------
 # our arm
 # ---------------------------------------------------------------------------
 
@@ -366,6 +420,7 @@ def ours(args, rank: int, world: int, local_rank: int) -> None:
     dom_ms = statistics.mean(per[dom_key])
     ach = nbytes[dom_key] / (dom_ms * 1e-3) / 1e9
 
+    side = side_measurements(dev, d16, inp["C"]) if world == 1 else None
     cpu_dt, cpu_by, cpu_desc = oracle_sample(inp, *CPU_SAMPLE)
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms,
@@ -388,6 +443,8 @@ def ours(args, rank: int, world: int, local_rank: int) -> None:
             # and its fix-up pass
             "gpu_launches": 4 * args.steps,
             "clocks": clk}
+    if side is not None:
+        line["unfused_and_dynamic"] = side
     print(json.dumps(line), flush=True)
 
 

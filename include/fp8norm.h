@@ -4,6 +4,7 @@
  * C ABI.  Every operation takes caller-owned DEVICE pointers, plain sizes and
  * strides (in elements), and the caller's cudaStream_t; it validates its
  * arguments on the host, enqueues its work on that stream (one kernel; the
+ * fused gated quantisation: its kernel and a short fix-up kernel; the
  * dynamic per-head quantisation: a memset and two kernels) and returns
  * without synchronising, so the calls can be captured in a CUDA graph.
  * The operations allocate no memory and keep no state between calls.
@@ -82,6 +83,10 @@ uint32_t fp8n_version(void);
  * Per token (one scale over all H*D values):
  *   scale[t] = RN32(max|y| / 448);  out[t, h*D + d] = e4m3(RN32(y / scale[t]))
  * A token with max|y| == 0 gets scale 0 and zero codes carrying the sign of y.
+ * The mean square is the exact one: a head whose fast double-float sum cannot
+ * decide RN32(S / D) is recomputed by a second kernel of the same call, which
+ * finds it through a temporary mark in scale[t] (a negative NaN that no scale
+ * can be); scale and out are final when the call's work completes.
  *
  * x, gate : bf16 [T, H, D]; heads contiguous inside a token; token strides
  *           x_stride / gate_stride (elements, multiples of 8, >= H*D).

@@ -169,14 +169,22 @@ struct TokenQuant {
   }
 };
 
-// The exact mean square of the heads flagged in a warp: every lane sums its
-// `count` chunks at p in double-double, the TPH lanes of a head combine their
-// sums, and a flagged lane steps ms to RN32(S / D).  Called by the whole warp.
+// The exact mean square of the heads flagged in a warp (D a power of two):
+// from the heads' sums of squares in 128-bit integers, or, for a head whose
+// exponents span too much for that, in double-double (every lane sums its
+// `count` chunks at p, the TPH lanes of a head combine), from which a flagged
+// lane steps ms to RN32(S / D).  Called by the whole warp.
 static __device__ __noinline__ float head_ms_exact(const uint4* p, int count, int tph, int D,
                                                    float ms, bool flagged) {
+  int log2d = 0;
+  while ((1 << log2d) < D) ++log2d;
+  float mi = ms;
+  const bool ok = head_ms_int(p, 1, count, tph, log2d, &mi);
+  if (!__any_sync(0xFFFFFFFFu, flagged && !ok)) return flagged ? mi : ms;
   dd Sd = sumsq_dd(p, 1, count);
   for (int m = 1; m < tph; m <<= 1) Sd = dd_add(Sd, shfl_xor_dd(Sd, m));
-  return flagged ? ms_resolve(Sd, (float)D, ms) : ms;
+  if (!flagged) return ms;
+  return ok ? mi : ms_resolve(Sd, (float)D, ms);
 }
 
 // Sum of squares of a head in the staged layout, from the thread's segment

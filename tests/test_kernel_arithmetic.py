@@ -359,3 +359,74 @@ def test_binary32_resolve_of_exact_sums():
             for k in (-2, -1, 0, 1, 2):
                 start = X.f32_bits_to_frac(_bits(want) + k)
                 assert _resolve_exact((h, l), n, start) == want, (n, S, k)
+
+
+def _ms_int(bits, log2n):
+    """The kernels' integer mean square, step by step: squares as integers
+    m^2 4^(e - emin), their sum rounded to binary32 at scale
+    2^(2(emin - 134) - log2n); None when the exponents span too much."""
+    nz = [b for b in bits if b & 0x7FFF]
+    if not nz:
+        return Fraction(0)
+    e1 = lambda b: max((b >> 7) & 0xFF, 1)
+    emin, emax = min(map(e1, nz)), max(map(e1, nz))
+    if 2 * (emax - emin) > 98:
+        return None
+    acc = 0
+    for b in nz:
+        m = (b & 0x7F) | (0x80 if b & 0x7F80 else 0)
+        acc += (m * m) << (2 * (e1(b) - emin))
+    base = 2 * (emin - 134) - log2n
+    msb = acc.bit_length() - 1
+    eres = msb + base
+    if eres > 127:
+        return None  # infinity
+    q = max(eres - 23, -149)
+    sh = q - base
+    if sh <= 0:
+        M = acc << -sh
+    else:
+        M, rem, half = acc >> sh, acc & ((1 << sh) - 1), 1 << (sh - 1)
+        if rem > half or (rem == half and M & 1):
+            M += 1
+    return M * Fraction(2) ** q
+
+
+def test_integer_mean_square_is_the_rounding_of_the_exact_sum():
+    """The integer path equals RN32(S / 2^k) of the exact sum on heads with
+    wide exponent spreads, subnormals, zeros and exact ties."""
+    import random
+    rng = random.Random(41)
+    cases = 0
+    for _ in range(400):
+        n = rng.choice((8, 16, 128))
+        lo = rng.randrange(1, 200)
+        hi = min(254, lo + rng.randrange(0, 50))
+        sub = 0.05 if lo < 40 else 0.0                       # subnormals with small exponents
+        bits = []
+        for _ in range(n):
+            r = rng.random()
+            if r < 0.1:
+                bits.append(0)
+            elif r < 0.1 + sub:
+                bits.append(rng.randrange(1, 0x80))          # subnormal
+            else:
+                bits.append((rng.randrange(lo, hi + 1) << 7) | rng.randrange(0, 128))
+        log2n = n.bit_length() - 1
+        got = _ms_int(bits, log2n)
+        if got is None:
+            continue
+        S = sum((X.bf16_to_frac(b) ** 2 for b in bits), Fraction(0))
+        assert got == X.round_rne(S / n, 24, -126), (bits, log2n)
+        cases += 1
+    for hx in TIE_HEADS_HOST:
+        S = sum((X.bf16_to_frac(b) ** 2 for b in hx), Fraction(0))
+        assert _ms_int(hx, 3) == X.round_rne(S / 8, 24, -126)
+    assert cases > 300
+
+
+# heads whose exact mean square is a binary32 tie, and the same plus a 2^-40
+TIE_HEADS_HOST = [
+    [0x3F93, 0x3F98, 0x3D37, 0x3D37, 0, 0, 0, 0],
+    [0x3F93, 0x3F98, 0x3D37, 0x3D37, 0x2B80, 0, 0, 0],
+]
