@@ -672,9 +672,10 @@ cudaError_t launch_tma_v(const GatedParams& p, cudaStream_t stream) {
 template <int MODE, int ACT, int CPT, int TPH>
 cudaError_t launch_tma(const GatedParams& p, cudaStream_t stream) {
   if (ModeOf<MODE>::gate) {
-    // the table costs about as much as 8192 / (H*D) tokens of activations per CTA
+    // filling the table costs about as much as 8192 activations computed in
+    // the arithmetic path; it pays when each CTA evaluates twice that many
     const int64_t per_cta = p.T / ((int64_t)sm_count() * 4);
-    if (per_cta * p.H * p.D >= 8 * kLutEntries)
+    if (per_cta * p.H * p.D >= 2 * kLutEntries)
       return launch_tma_v<MODE, ACT, CPT, TPH, true>(p, stream);
   }
   return launch_tma_v<MODE, ACT, CPT, TPH, false>(p, stream);
