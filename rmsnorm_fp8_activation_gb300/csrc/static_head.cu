@@ -8,7 +8,7 @@
 // GB300 design: an HBM stream (2 bytes in, 1 byte out per element).  Each
 // tensor is a flat sequence of 16-byte input chunks (8 elements of one head);
 // a persistent grid walks Q, then K, then V with 16-byte streaming loads,
-// kUnroll chunks in flight per thread, and writes 8-byte code chunks to the
+// kUnroll (6) chunks in flight per thread, and writes 8-byte code chunks to the
 // contiguous outputs.
 // Head indices come from a multiply-shift division (Granlund and Montgomery,
 // "Division by invariant integers using multiplication", PLDI 1994).  The
@@ -22,7 +22,7 @@ namespace fp8n {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kUnroll = 4;
+constexpr int kUnroll = 6;
 constexpr int kMaxHeads = 256;  // largest H taken (the API rejects more)
 
 // n / d for 0 <= n < 2^31: q = (umulhi(n, m) + n) >> l with l = ceil(log2 d)
