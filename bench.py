@@ -262,12 +262,41 @@ def side_measurements(dev, d16, inp_c) -> dict:
     b_unfused = timed(lambda: (B.fp8n_quant_mx(B.fp8n_rmsnorm_bf16(q, wq, wm.eps)),
                                B.fp8n_rmsnorm_bf16(kv, wkv, wm.eps)))
     dyn = timed(lambda: B.fp8n_dynamic_head_quant(Q, K, V))
+
+    # decode-sized (A) (56 tokens x 12 heads x 128), one call replayed from a
+    # CUDA graph, inputs resident (as in a decode loop): device time per call
+    wd = W["gated_small"]
+    xd, gd, wtd = d16(wd.x()), d16(wd.gate()), d16(wd.weight())
+    od = torch.empty((wd.T, wd.H * wd.D), dtype=torch.uint8, device=dev)
+    sd = torch.empty((wd.T,), dtype=torch.float32, device=dev)
+    cs = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(cs):
+        for _ in range(3):
+            B.fp8n_gated_rmsnorm_quant_token(xd, gd, wtd, wd.eps, wd.act, out=od, scale=sd)
+    cs.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=cs):
+        B.fp8n_gated_rmsnorm_quant_token(xd, gd, wtd, wd.eps, wd.act, out=od, scale=sd)
+    reps = 200
+    for _ in range(10):
+        graph.replay()
+    torch.cuda.synchronize()
+    g0 = torch.cuda.Event(enable_timing=True)
+    g1 = torch.cuda.Event(enable_timing=True)
+    g0.record()
+    for _ in range(reps):
+        graph.replay()
+    g1.record()
+    torch.cuda.synchronize()
+    small_us = 1e3 * g0.elapsed_time(g1) / reps
     n_c = Q.numel() + K.numel() + V.numel()
     return {
         "gated_silu_fused_us": a_fused, "gated_silu_unfused_us": a_unfused,
         "gated_silu_unfused_steps": "fp8n_gated_rmsnorm_bf16 -> fp8n_quant_token",
         "qkv_mx_fused_us": b_fused, "qkv_mx_unfused_us": b_unfused,
         "qkv_mx_unfused_steps": "fp8n_rmsnorm_bf16(q) -> fp8n_quant_mx; fp8n_rmsnorm_bf16(kv)",
+        "gated_small_graph_us": small_us,
+        "gated_small_graph_note": "56 x 12 x 128 sigmoid, one call per graph replay, inputs resident",
         "dynamic_head_quant_us": dyn,
         "dynamic_head_quant_GB_s": 5 * n_c / (dyn * 1e-6) / 1e9,
         "dynamic_head_quant_bytes": "2 B/element read twice, 1 B/element written",

@@ -83,10 +83,11 @@ uint32_t fp8n_version(void);
  * Per token (one scale over all H*D values):
  *   scale[t] = RN32(max|y| / 448);  out[t, h*D + d] = e4m3(RN32(y / scale[t]))
  * A token with max|y| == 0 gets scale 0 and zero codes carrying the sign of y.
- * The mean square is the exact one: a head whose fast double-float sum cannot
- * decide RN32(S / D) is recomputed by a second kernel of the same call, which
- * finds it through a temporary mark in scale[t] (a negative NaN that no scale
- * can be); scale and out are final when the call's work completes.
+ * The mean square is the exact one.  On long batches a head whose fast
+ * double-float sum cannot decide RN32(S / D) is recomputed by a second kernel
+ * of the same call, which finds it through a temporary mark in scale[t] (a
+ * negative NaN that no scale can be); scale and out are final when the call's
+ * work completes.
  *
  * x, gate : bf16 [T, H, D]; heads contiguous inside a token; token strides
  *           x_stride / gate_stride (elements, multiples of 8, >= H*D).

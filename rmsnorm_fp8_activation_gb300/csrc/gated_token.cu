@@ -312,10 +312,11 @@ __global__ void __launch_bounds__(512) gated_token_tma(const GatedParams p, int 
       unsure = S.h != 0.0f &&
                __fadd_rn(S.h, __fadd_rn(S.l, err)) != __fadd_rn(S.h, __fsub_rn(S.l, err));
       ms = __fmul_rn(__fadd_rn(S.h, S.l), inv_d);
-      // the bf16 output of the gated norm settles a flagged head here (an
-      // exact sum needs nothing more; otherwise a double-double sum over the
-      // row); the quantising kernel does so after pass 2 below
-      if (!M::quant && __any_sync(0xFFFFFFFFu, unsure)) {
+      // the bf16 output of the gated norm, and the quantisation of short
+      // batches (no gate table), settle a flagged head here (an exact sum
+      // needs nothing more; otherwise the integer path); the quantisation of
+      // long batches marks the token for its fix-up pass after pass 2 below
+      if ((!M::quant || !LUT) && __any_sync(0xFFFFFFFFu, unsure)) {
         const bool exact = head_sum_exact<CPT, TPH>(sx, active, S.h);  // every lane: shuffles
         unsure = unsure && !exact;
         if (__any_sync(0xFFFFFFFFu, unsure))
@@ -371,7 +372,7 @@ __global__ void __launch_bounds__(512) gated_token_tma(const GatedParams p, int 
       // a flagged head whose sum is exact is settled; any other marks the
       // token for the fix-up pass (see kRedoScale)
       bool wflag = false;
-      if (M::norm && __any_sync(0xFFFFFFFFu, unsure)) {
+      if (M::norm && LUT && __any_sync(0xFFFFFFFFu, unsure)) {
         const bool exact = head_sum_exact<CPT, TPH>(sx, active, Sh);  // every lane: shuffles
         wflag = __any_sync(0xFFFFFFFFu, unsure && !exact);
       }
@@ -665,7 +666,7 @@ cudaError_t launch_tma_v(const GatedParams& p, cudaStream_t stream) {
   const int grid = (int)(p.T < want ? p.T : want);
   kern<<<grid, block, smem, stream>>>(p, nstage);
   e = cudaGetLastError();
-  if (e != cudaSuccess || MODE != kModeNormQuant) return e;
+  if (e != cudaSuccess || MODE != kModeNormQuant || !LUT) return e;
   return launch_fixup<ACT, CPT, TPH>(p, stream);  // tokens marked with kRedoScale
 }
 
