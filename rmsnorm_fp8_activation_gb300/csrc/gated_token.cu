@@ -256,15 +256,6 @@ __global__ void __launch_bounds__(512) gated_token_tma(const GatedParams p, int 
   uint16_t* wsm = reinterpret_cast<uint16_t*>(smem + kHeader + (LUT ? kLutBytes : 0));  // weight [D]
   uint8_t* stages = smem + kHeader + (LUT ? kLutBytes : 0) + (M::norm ? 2 * p.D : 0);
 
-  if (M::norm)
-    for (int i = tid; i < p.D / 8; i += blockDim.x)
-      reinterpret_cast<uint4*>(wsm)[i] = reinterpret_cast<const uint4*>(p.weight)[i];
-  if (tid == 0) {
-    for (int s = 0; s < nstage; ++s) mbar_init(smem_u32(&bars[s]), 1);
-    asm volatile("fence.mbarrier_init.release.cluster;\n fence.proxy.async.shared::cta;" ::: "memory");
-  }
-  __syncthreads();
-
   auto issue = [&](int s, int64_t t) {
     uint32_t bar = smem_u32(&bars[s]);
     uint32_t dst = smem_u32(stages + (size_t)s * stage_bytes);
@@ -272,11 +263,20 @@ __global__ void __launch_bounds__(512) gated_token_tma(const GatedParams p, int 
     bulk_g2s(dst, p.x + t * p.x_stride, row_bytes, bar);
     if (M::gate) bulk_g2s(dst + row_bytes, p.gate + t * p.gate_stride, row_bytes, bar);
   };
-  if (tid == 0)
+  // the first rows are requested before anything else, so that their copies
+  // overlap the weight load and the table fill
+  if (tid == 0) {
+    for (int s = 0; s < nstage; ++s) mbar_init(smem_u32(&bars[s]), 1);
+    asm volatile("fence.mbarrier_init.release.cluster;\n fence.proxy.async.shared::cta;" ::: "memory");
     for (int s = 0; s < nstage; ++s) {
       int64_t t = blockIdx.x + (int64_t)s * gridDim.x;
       if (t < p.T) issue(s, t);
     }
+  }
+  if (M::norm)
+    for (int i = tid; i < p.D / 8; i += blockDim.x)
+      reinterpret_cast<uint4*>(wsm)[i] = reinterpret_cast<const uint4*>(p.weight)[i];
+  __syncthreads();
   if (LUT) {  // filled while the first rows are in flight
     lut_fill<ACT>(reinterpret_cast<uint32_t*>(lut), tid, blockDim.x);
     __syncthreads();
