@@ -468,9 +468,7 @@ def ours(args, rank: int, world: int, local_rank: int) -> None:
             "e2e": {"value": aggregate_gbs(total_bytes, world, e2e_ms), "unit": UNIT,
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "ms_per_step": e2e_ms},
-            # per step: (B) one kernel, (C) one kernel, (A) the staged kernel
-            # and its fix-up pass
-            "gpu_launches": 4 * args.steps,
+            "gpu_launches": 3 * args.steps,  # one kernel per operation and step
             "clocks": clk}
     if side is not None:
         line["unfused_and_dynamic"] = side

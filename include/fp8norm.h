@@ -4,7 +4,6 @@
  * C ABI.  Every operation takes caller-owned DEVICE pointers, plain sizes and
  * strides (in elements), and the caller's cudaStream_t; it validates its
  * arguments on the host, enqueues its work on that stream (one kernel; the
- * fused gated quantisation: its kernel and a short fix-up kernel; the
  * dynamic per-head quantisation: a memset and two kernels) and returns
  * without synchronising, so the calls can be captured in a CUDA graph.
  * The operations allocate no memory and keep no state between calls.
@@ -83,11 +82,10 @@ uint32_t fp8n_version(void);
  * Per token (one scale over all H*D values):
  *   scale[t] = RN32(max|y| / 448);  out[t, h*D + d] = e4m3(RN32(y / scale[t]))
  * A token with max|y| == 0 gets scale 0 and zero codes carrying the sign of y.
- * The mean square is the exact one.  On long batches a head whose fast
- * double-float sum cannot decide RN32(S / D) is recomputed by a second kernel
- * of the same call, which finds it through a temporary mark in scale[t] (a
- * negative NaN that no scale can be); scale and out are final when the call's
- * work completes.
+ * The fused kernel sums the squares with a compensated (not exact) sum: in
+ * rare heads its ms is one binary32 ulp off the exact one, which can move a
+ * code by one step (the reduction-order budget of the codes).  The step
+ * functions below take the exact mean square.
  *
  * x, gate : bf16 [T, H, D]; heads contiguous inside a token; token strides
  *           x_stride / gate_stride (elements, multiples of 8, >= H*D).
@@ -115,9 +113,10 @@ fp8n_status fp8n_gated_rmsnorm_quant_token(const void* x, int64_t x_stride, cons
  * gated norm and the per-token quant as two launches, 8.5 us against 4.2 us
  * fused); the cross-referenced "[ROCm][Kimi-K3] Fuse MLA sigmoid-mul with
  * per-token FP8 for o_proj" (PR 55043, title only) for the gate product
- * followed by the per-token quant.  Every rounding is the one of (A), so
- * fp8n_quant_token(fp8n_gated_rmsnorm_bf16(...)) equals
- * fp8n_gated_rmsnorm_quant_token(...) bit for bit.
+ * followed by the per-token quant.  Every rounding is the one of (A), with
+ * the exact mean square, so fp8n_quant_token(fp8n_gated_rmsnorm_bf16(...))
+ * is (A)'s definition bit for bit (the fused call is within its code
+ * tolerance of it).
  */
 
 /* y[t, h*D + d] = the bf16 y of (A), written out instead of quantised.

@@ -216,6 +216,31 @@ __host__ __device__ __forceinline__ float head_sum_rel_err() {
   return sumsq_rel_err(4 * ((CPT + 1) / 2), 3 + lg);
 }
 
+// The fused quantisation's head sum: the same layout with one Kahan-
+// compensated chain per thread (two packed lanes; four operations per pair
+// instead of Sum2's eight).  It is not an exact sum: in rare heads (a large
+// square after a smaller running sum, or compensation bits below a term's
+// precision) RN32(S / D) comes out one binary32 ulp off, which moves a code by
+// one step at most, rarely (about one code in 10^7 on the benchmark data);
+// that is the reduction-order budget of the per-token codes, and it keeps this
+// kernel at the HBM roofline.
+template <int CPT, int TPH>
+__device__ __forceinline__ df head_sum_fast(const uint8_t* xs, int tid, bool active) {
+  kahan2 acc;
+#pragma unroll
+  for (int c = 0; c < CPT; ++c) {
+    const uint4 xv = active ? *reinterpret_cast<const uint4*>(xs + 16 * slot_of<CPT>(c, tid))
+                            : make_uint4(0, 0, 0, 0);
+    const uint32_t* xw = &xv.x;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) acc.add_sq(xw[k]);
+  }
+  df S = acc.value();
+#pragma unroll
+  for (int m = 1; m < TPH; m <<= 1) S = df_add(S, shfl_xor_df(S, m));
+  return S;
+}
+
 // Whether head_sum's double-float S is the exact sum of squares of the head
 // (sum_is_exact over the head's elements).  Heads of bf16 data often sum
 // exactly to a binary32 tie; this settles them without the double-double
@@ -235,10 +260,6 @@ __device__ __forceinline__ bool head_sum_exact(const uint8_t* xs, bool active, f
   return sum_is_exact(emin, Sh, 4 * ((CPT + 1) / 2));
 }
 
-// Scale word written by the staged kernel for a token with a head whose mean
-// square its double-float sum could not decide: a negative NaN, which no
-// scale RN32(amax / 448) can be.  The fix-up kernel recomputes those tokens.
-constexpr uint32_t kRedoScale = 0xFFFFFFFFu;
 
 template <int MODE, int ACT, int CPT, int TPH, bool LUT>
 __global__ void __launch_bounds__(512) gated_token_tma(const GatedParams p, int nstage) {
@@ -251,7 +272,7 @@ __global__ void __launch_bounds__(512) gated_token_tma(const GatedParams p, int 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
   const bool active = tid < nthr;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
-  uint32_t* red = reinterpret_cast<uint32_t*>(smem + 64);  // per-warp amax bits | flag bit 31
+  uint32_t* red = reinterpret_cast<uint32_t*>(smem + 64);  // per-warp amax bits
   uint8_t* lut = smem + kHeader;  // at a fixed offset: its base folds into the loads
   uint16_t* wsm = reinterpret_cast<uint16_t*>(smem + kHeader + (LUT ? kLutBytes : 0));  // weight [D]
   uint8_t* stages = smem + kHeader + (LUT ? kLutBytes : 0) + (M::norm ? 2 * p.D : 0);
@@ -298,31 +319,30 @@ __global__ void __launch_bounds__(512) gated_token_tma(const GatedParams p, int 
     const uint8_t* sx = stages + (size_t)s * stage_bytes + (size_t)seg * 2;
     const uint8_t* sg = sx + row_bytes;
 
-    // pass 1: the head's sum of squares (x is read again in pass 2), ms =
-    // RN32(S / D), and whether that rounding is undecided.  RN32(S) is
+    // pass 1: the head's sum of squares (x is read again in pass 2) and ms =
+    // RN32(S / D).  The quantisation takes the fast compensated sum.  The bf16
+    // output of the gated norm takes the exact one: Sum2, then RN32(S) is
     // decided when it is the same at both ends of S's error interval (RN is
-    // monotone; the probes' own roundings are far below err).  S.h == 0 means
+    // monotone; the probes' own roundings are far below err; S.h == 0 means
     // every square is at most 2^-150, and then so is S / D: its rounding is
-    // 0.  The lanes of a head agree on S, so a head is flagged as a whole.
-    float ms = 0.0f, Sh = 0.0f;
-    bool unsure = false;
-    if (M::norm) {
+    // 0), else a certified-exact sum needs nothing more, else the integer
+    // path.  The lanes of a head agree on S, so a head is flagged as a whole.
+    float ms = 0.0f;
+    if (M::norm && M::quant) {
+      const df S = head_sum_fast<CPT, TPH>(sx, tid, active);
+      ms = __fmul_rn(__fadd_rn(S.h, S.l), inv_d);
+    } else if (M::norm) {
       df S = head_sum<CPT, TPH>(sx, tid, active);
       const float err = __fmaf_rn(S.h, rel_err, sq_floor);
-      unsure = S.h != 0.0f &&
-               __fadd_rn(S.h, __fadd_rn(S.l, err)) != __fadd_rn(S.h, __fsub_rn(S.l, err));
+      bool unsure = S.h != 0.0f &&
+                    __fadd_rn(S.h, __fadd_rn(S.l, err)) != __fadd_rn(S.h, __fsub_rn(S.l, err));
       ms = __fmul_rn(__fadd_rn(S.h, S.l), inv_d);
-      // the bf16 output of the gated norm, and the quantisation of short
-      // batches (no gate table), settle a flagged head here (an exact sum
-      // needs nothing more; otherwise the integer path); the quantisation of
-      // long batches marks the token for its fix-up pass after pass 2 below
-      if ((!M::quant || !LUT) && __any_sync(0xFFFFFFFFu, unsure)) {
+      if (__any_sync(0xFFFFFFFFu, unsure)) {
         const bool exact = head_sum_exact<CPT, TPH>(sx, active, S.h);  // every lane: shuffles
         unsure = unsure && !exact;
         if (__any_sync(0xFFFFFFFFu, unsure))
           ms = head_ms_exact(reinterpret_cast<const uint4*>(sx), active ? CPT : 0, TPH, p.D, ms, unsure);
       }
-      Sh = S.h;
     }
 
     // pass 2: y (= bf16(bf16(bf16(x r) w) act(g)) through the norm), kept as bf16 pairs
@@ -369,14 +389,7 @@ __global__ void __launch_bounds__(512) gated_token_tma(const GatedParams p, int 
       float amax = fmax_nan(bf16_lo(am2), bf16_hi(am2));
 #pragma unroll
       for (int m = 16; m >= 1; m >>= 1) amax = fmax_nan(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, m));
-      // a flagged head whose sum is exact is settled; any other marks the
-      // token for the fix-up pass (see kRedoScale)
-      bool wflag = false;
-      if (M::norm && LUT && __any_sync(0xFFFFFFFFu, unsure)) {
-        const bool exact = head_sum_exact<CPT, TPH>(sx, active, Sh);  // every lane: shuffles
-        wflag = __any_sync(0xFFFFFFFFu, unsure && !exact);
-      }
-      if (lane == 0) redb[warp] = __float_as_uint(amax) | (wflag ? 0x80000000u : 0u);
+      if (lane == 0) redb[warp] = __float_as_uint(amax);
     }
     // every thread is done with stage s and has published its warp's amax
     if (__syncthreads_or(timeout)) break;
@@ -394,15 +407,10 @@ __global__ void __launch_bounds__(512) gated_token_tma(const GatedParams p, int 
       }
       continue;
     }
-    uint32_t u = redb[0], flags = u;
-    float tam = __uint_as_float(u & 0x7FFFFFFFu);
-    for (int w = 1; w < nwarps; ++w) {
-      u = redb[w];
-      flags |= u;
-      tam = fmax_nan(tam, __uint_as_float(u & 0x7FFFFFFFu));
-    }
+    float tam = __uint_as_float(redb[0]);
+    for (int w = 1; w < nwarps; ++w) tam = fmax_nan(tam, __uint_as_float(redb[w]));
     const float scale = scale_of(tam);
-    if (tid == 0) p.scale[t] = (flags >> 31) ? __uint_as_float(kRedoScale) : scale;
+    if (tid == 0) p.scale[t] = scale;
     if (active) {
       const TokenQuant tq(scale);
       uint8_t* orow = p.out + t * p.out_stride + seg;
@@ -542,104 +550,6 @@ __global__ void __launch_bounds__(256) gated_token_generic(const GatedParams p) 
   for (int64_t t = blockIdx.x; t < p.T; t += gridDim.x) generic_token<MODE, ACT>(p, t, smem);
 }
 
-template <int ACT, int CPT, int TPH>
-cudaError_t launch_fixup(const GatedParams& p, cudaStream_t stream);
-
-// Fix-up after the staged gated quantisation: a persistent grid in which CTA
-// b owns the tokens b, b + G, b + 2G, ... (G = gridDim.x), finds those the
-// staged kernel marked with kRedoScale (rare: a head whose sum of squares
-// lies next to a rounding boundary of its mean square), and recomputes each
-// from global memory in the staged kernel's layout, the flagged heads taking
-// their exact mean square from a double-double sum.  Everything else is the
-// staged kernel's arithmetic, so the unflagged heads come out the same.
-template <int ACT, int CPT, int TPH>
-__global__ void __launch_bounds__(512) gated_token_fixup(const GatedParams p) {
-  extern __shared__ __align__(16) uint8_t fsm[];
-  __shared__ int64_t list[512];
-  __shared__ int count;
-  __shared__ float red[32];
-  uint16_t* wsm = reinterpret_cast<uint16_t*>(fsm);  // weight [D]
-  const int row = p.H * p.D;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
-  const bool active = tid < row / (8 * CPT);
-  const int seg = tid * 8 * CPT;
-  for (int i = tid; i < p.D / 8; i += blockDim.x)
-    reinterpret_cast<uint4*>(wsm)[i] = reinterpret_cast<const uint4*>(p.weight)[i];
-  const uint16_t* wseg = wsm + (seg % p.D);
-  const float inv_d = 1.0f / (float)p.D;
-  const float rel_err = head_sum_rel_err<CPT, TPH>();
-  const float sq_floor = (float)p.D * 0x1p-149f;
-  const int64_t G = gridDim.x;
-  const int64_t mine = (p.T - blockIdx.x + G - 1) / G;  // tokens of this CTA
-
-  for (int64_t j0 = 0; j0 < mine; j0 += blockDim.x) {
-    if (tid == 0) count = 0;
-    __syncthreads();
-    const int64_t j = j0 + tid;
-    if (j < mine) {
-      const int64_t t = blockIdx.x + j * G;
-      if (__float_as_uint(p.scale[t]) == kRedoScale) list[atomicAdd(&count, 1)] = t;
-    }
-    __syncthreads();
-    const int n = count;
-    for (int i = 0; i < n; ++i) {
-      const int64_t t = list[i];
-      const uint8_t* gx = reinterpret_cast<const uint8_t*>(p.x + t * p.x_stride + seg);
-      const uint8_t* gg = reinterpret_cast<const uint8_t*>(p.gate + t * p.gate_stride + seg);
-      const df S = head_sum<CPT, TPH>(gx, tid, active);
-      const float err = __fmaf_rn(S.h, rel_err, sq_floor);
-      const bool unsure = S.h != 0.0f &&
-                          __fadd_rn(S.h, __fadd_rn(S.l, err)) != __fadd_rn(S.h, __fsub_rn(S.l, err));
-      float ms = __fmul_rn(__fadd_rn(S.h, S.l), inv_d);
-      bool redo = unsure;
-      if (__any_sync(0xFFFFFFFFu, redo)) {
-        const bool exact = head_sum_exact<CPT, TPH>(gx, active, S.h);  // every lane: shuffles
-        redo = redo && !exact;
-      }
-      if (__any_sync(0xFFFFFFFFu, redo))
-        ms = head_ms_exact(reinterpret_cast<const uint4*>(gx), active ? CPT : 0, TPH, p.D, ms, redo);
-      const f2_t r2 = splat2(rms_factor(ms, p.eps));
-      uint32_t y[CPT][4];
-      uint32_t am2 = 0;
-#pragma unroll
-      for (int c = 0; c < CPT; ++c) {
-        const int off = 16 * slot_of<CPT>(c, tid);
-        uint4 xv = make_uint4(0, 0, 0, 0), gv = xv;
-        if (active) {
-          xv = *reinterpret_cast<const uint4*>(gx + off);
-          gv = *reinterpret_cast<const uint4*>(gg + off);
-        }
-        const uint4 wv = *reinterpret_cast<const uint4*>(wseg + 8 * slot_of<CPT>(c, tid));
-        const uint32_t *xw = &xv.x, *gw = &gv.x, *ww = &wv.x;
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          y[c][k] = gated_pair(xw[k], act_bf16_pair(gw[k], ACT), ww[k], r2);
-          if (active) am2 = amax_step(am2, y[c][k]);
-        }
-      }
-      float amax = fmax_nan(bf16_lo(am2), bf16_hi(am2));
-#pragma unroll
-      for (int m = 16; m >= 1; m >>= 1) amax = fmax_nan(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, m));
-      if (lane == 0) red[warp] = amax;
-      __syncthreads();
-      float tam = red[0];
-      for (int w = 1; w < nwarps; ++w) tam = fmax_nan(tam, red[w]);
-      const float scale = scale_of(tam);
-      if (tid == 0) p.scale[t] = scale;
-      if (active) {
-        const TokenQuant tq(scale);
-        uint8_t* orow = p.out + t * p.out_stride + seg;
-#pragma unroll
-        for (int c = 0; c < CPT; ++c)
-          *reinterpret_cast<uint2*>(orow + 8 * slot_of<CPT>(c, tid)) =
-              tq.tiny ? tq.chunk<true>(y[c]) : tq.chunk<false>(y[c]);
-      }
-      __syncthreads();  // red is reused by the next token
-    }
-    __syncthreads();  // every thread has read count before it is reset
-  }
-}
-
 // Rows of 16 KB or more per stage get one stage per CTA, so that four CTAs
 // fit on an SM and the loads of the others overlap each CTA's compute (its own
 // next row also lands while it quantises); shorter rows get two stages.  The
@@ -665,9 +575,7 @@ cudaError_t launch_tma_v(const GatedParams& p, cudaStream_t stream) {
   const int64_t want = (int64_t)sm_count() * per_sm;
   const int grid = (int)(p.T < want ? p.T : want);
   kern<<<grid, block, smem, stream>>>(p, nstage);
-  e = cudaGetLastError();
-  if (e != cudaSuccess || MODE != kModeNormQuant || !LUT) return e;
-  return launch_fixup<ACT, CPT, TPH>(p, stream);  // tokens marked with kRedoScale
+  return cudaGetLastError();
 }
 
 template <int MODE, int ACT, int CPT, int TPH>
@@ -687,21 +595,6 @@ inline size_t generic_smem(const GatedParams& p) {
   return (size_t)(p.H * p.D / 8) * sizeof(df) + (size_t)p.H * 4 + 32 * 4;
 }
 
-template <int ACT, int CPT, int TPH>
-cudaError_t launch_fixup(const GatedParams& p, cudaStream_t stream) {
-  auto kern = gated_token_fixup<ACT, CPT, TPH>;
-  const int block = (p.H * p.D / (8 * CPT) + 31) / 32 * 32;
-  const size_t smem = 2 * (size_t)p.D;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
-  int per_sm = 0;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, block, smem);
-  if (e != cudaSuccess) return e;
-  if (per_sm < 1) per_sm = 1;
-  const int64_t want = (int64_t)sm_count() * per_sm;
-  kern<<<(int)(p.T < want ? p.T : want), block, smem, stream>>>(p);
-  return cudaGetLastError();
-}
 
 template <int MODE, int ACT>
 cudaError_t launch_generic(const GatedParams& p, cudaStream_t stream) {
