@@ -623,13 +623,18 @@ cudaError_t dispatch(const GatedParams& p, cudaStream_t stream) {
     return launch_generic<MODE, ACT>(p, stream);
   }
   // staged kernel: D/8 a power of two, a head spans at most a warp, the row
-  // fits one CTA and a stage fits shared memory
-  const int cpt = p.D >= 32 ? 4 : p.D / 8;
+  // fits one CTA and a stage fits shared memory.  A batch that gives each CTA
+  // at most one token (decode) spreads a D = 128 head over 16 lanes of one
+  // chunk each instead of 4 lanes of four: shorter chains per thread, the
+  // same arithmetic.
+  int cpt = p.D >= 32 ? 4 : p.D / 8;
+  if (p.D == 128 && p.T <= sm_count() && row / 8 <= 512) cpt = 1;
   const int tph = p.D / (8 * cpt);
   const bool pow2 = (p.D & (p.D - 1)) == 0;
   if (pow2 && tph >= 1 && tph <= 32 && row / (8 * cpt) <= 512 && 4 * row <= 64 * 1024) {
     switch (cpt * 100 + tph) {
       case 101: return launch_tma<MODE, ACT, 1, 1>(p, stream);
+      case 116: return launch_tma<MODE, ACT, 1, 16>(p, stream);
       case 201: return launch_tma<MODE, ACT, 2, 1>(p, stream);
       case 401: return launch_tma<MODE, ACT, 4, 1>(p, stream);
       case 402: return launch_tma<MODE, ACT, 4, 2>(p, stream);
