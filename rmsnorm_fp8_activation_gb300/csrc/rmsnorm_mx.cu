@@ -280,7 +280,7 @@ __device__ __forceinline__ uint32_t mx_code(uint32_t A) {
 // reads chunks l, l+32, ... of the slot (consecutive 16-byte words: no bank
 // conflicts) in both passes.
 constexpr int kSlots = 2;
-constexpr int kStagedMaxWarps = 16;
+constexpr int kStagedMaxWarps = 32;
 // mbarriers of every warp (8 bytes per slot), ahead of the row slots
 constexpr int kStagedHeader = kStagedMaxWarps * kSlots * 8;
 static_assert(kStagedHeader % 128 == 0, "row slots start 128-byte aligned");
@@ -412,7 +412,7 @@ __global__ void __launch_bounds__(kStagedMaxWarps * 32) rmsnorm_mx_tma(const MxP
   }
 }
 
-// Warps per CTA: the count (up to 16) whose CTAs pack the most warps into an
+// Warps per CTA: the count (up to 32) whose CTAs pack the most warps into an
 // SM's shared memory (two row slots per warp); a row per warp-slot pair keeps
 // the slowest warp at as few rows as the SM count allows.
 cudaError_t launch_staged(const MxParams& p, cudaStream_t stream) {
