@@ -71,6 +71,9 @@ def load_library(path: str) -> ctypes.CDLL:
     L.oracle_gated_rmsnorm_quant_one.argtypes = [
         P, P, P, i32, i32, f32, ctypes.c_int, P, P, P]
     L.oracle_gated_rmsnorm_quant_one.restype = None
+    L.oracle_gated_rmsnorm_quant_one_ms.argtypes = [
+        P, P, P, i32, i32, f32, ctypes.c_int, P, P, P, P]
+    L.oracle_gated_rmsnorm_quant_one_ms.restype = None
     L.oracle_rmsnorm_quant_mx.argtypes = [
         P, i64, P, i32, P, i64, P, i32, i64, f32, P, i64, P, i64, P, i64]
     L.oracle_rmsnorm_quant_mx.restype = None
@@ -99,6 +102,32 @@ def _ptr(a: np.ndarray) -> int:
 
 def _c(a, dtype) -> np.ndarray:
     return np.ascontiguousarray(a, dtype=dtype)
+
+
+def host_threads() -> int:
+    """Host threads available to this process."""
+    try:
+        return max(1, len(os.sched_getaffinity(0)))
+    except AttributeError:  # not on Linux
+        return max(1, os.cpu_count() or 1)
+
+
+def sliced(fn, n: int, threads: int | None = None, min_slice: int = 1):
+    """Run ``fn(start, stop)`` over [0, n) cut into contiguous slices, on a
+    pool of host threads (the oracle's functions are called through ctypes,
+    which releases the interpreter lock, so the slices run in parallel; each
+    call is the same single-threaded function on its own rows).  Returns the
+    results in slice order.  threads=1 runs the slices in order on the calling
+    thread."""
+    from concurrent.futures import ThreadPoolExecutor
+    threads = host_threads() if threads is None else max(1, int(threads))
+    lib()  # load once, before the pool
+    parts = min(max(1, n // max(1, min_slice)), 4 * threads) if n > 0 else 0
+    bounds = [(n * i // parts, n * (i + 1) // parts) for i in range(parts)]
+    if threads == 1 or parts <= 1:
+        return [fn(a, b) for a, b in bounds]
+    with ThreadPoolExecutor(max_workers=threads) as ex:
+        return list(ex.map(lambda ab: fn(*ab), bounds))
 
 
 # ---- codecs ---------------------------------------------------------------
@@ -199,6 +228,28 @@ def gated_rmsnorm_quant_one(x_tok, gate_tok, weight, eps: float, act: int):
     scale = np.zeros((1,), dtype=np.float32)
     lib().oracle_gated_rmsnorm_quant_one(
         _ptr(x_tok), _ptr(gate_tok), _ptr(weight), H, D, float(eps), int(act),
+        _ptr(y), _ptr(out), _ptr(scale))
+    return y, out, float(scale[0])
+
+
+def gated_rmsnorm_quant_one_ms(x_tok, gate_tok, weight, eps: float, act: int, ms):
+    """Operation (A) on one token with each head's mean square given (float32
+    [H]) instead of computed: a diagnostic that the parity checks use to tell
+    whether a differing token is explained by one head's summation order.
+
+    Returns (y bf16 bits [H*D], codes uint8 [H*D], scale float).
+    """
+    x_tok = _c(x_tok, np.uint16)
+    gate_tok = _c(gate_tok, np.uint16)
+    weight = _c(weight, np.uint16)
+    ms = _c(ms, np.float32)
+    H, D = x_tok.shape
+    assert ms.shape == (H,)
+    y = np.zeros((H * D,), dtype=np.uint16)
+    out = np.zeros((H * D,), dtype=np.uint8)
+    scale = np.zeros((1,), dtype=np.float32)
+    lib().oracle_gated_rmsnorm_quant_one_ms(
+        _ptr(x_tok), _ptr(gate_tok), _ptr(weight), H, D, float(eps), int(act), _ptr(ms),
         _ptr(y), _ptr(out), _ptr(scale))
     return y, out, float(scale[0])
 

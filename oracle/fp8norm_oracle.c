@@ -261,14 +261,17 @@ void oracle_quant_row(const uint16_t* y, int64_t n, uint8_t* out, float* scale_o
   }
 }
 
-/* y = bf16(bf16(bf16(RN32(x * r)) * w) * bf16(act(g))) for one token, heads of D. */
-void oracle_gated_rmsnorm_row(const uint16_t* x_tok, const uint16_t* gate_tok,
-                              const uint16_t* weight, int32_t H, int32_t D, float eps, int act,
-                              uint16_t* y_tok) {
+/* y = bf16(bf16(bf16(RN32(x * r)) * w) * bf16(act(g))) for one token, heads of D.
+ * ms_given: NULL, or the mean square of each head to use in place of the exact
+ * one (a diagnostic input; see oracle_gated_rmsnorm_quant_one_ms). */
+static void gated_rmsnorm_row_ms(const uint16_t* x_tok, const uint16_t* gate_tok,
+                                 const uint16_t* weight, int32_t H, int32_t D, float eps, int act,
+                                 const float* ms_given, uint16_t* y_tok) {
   for (int32_t h = 0; h < H; ++h) {
     const uint16_t* xh = x_tok + (int64_t)h * D;
     const uint16_t* gh = gate_tok + (int64_t)h * D;
-    float r = oracle_rms_factor(oracle_mean_square_bf16(xh, D), eps);
+    float ms = ms_given ? ms_given[h] : oracle_mean_square_bf16(xh, D);
+    float r = oracle_rms_factor(ms, eps);
     for (int32_t d = 0; d < D; ++d) {
       uint16_t u = norm_times_weight(xh[d], r, weight[d]);
       uint16_t g = oracle_act_bf16(gh[d], act);
@@ -276,6 +279,25 @@ void oracle_gated_rmsnorm_row(const uint16_t* x_tok, const uint16_t* gate_tok,
           oracle_bf16_from_double(oracle_bf16_to_double(u) * oracle_bf16_to_double(g));
     }
   }
+}
+
+void oracle_gated_rmsnorm_row(const uint16_t* x_tok, const uint16_t* gate_tok,
+                              const uint16_t* weight, int32_t H, int32_t D, float eps, int act,
+                              uint16_t* y_tok) {
+  gated_rmsnorm_row_ms(x_tok, gate_tok, weight, H, D, eps, act, NULL, y_tok);
+}
+
+/* (A) on one token with each head's mean square given instead of computed.
+ * Not part of the definition: the parity checks call it with a head's exact
+ * ms moved by a unit or two in the last place, to tell whether a token on
+ * which the fused kernel differs is explained by that head's summation
+ * order alone (every other step unchanged). */
+void oracle_gated_rmsnorm_quant_one_ms(const uint16_t* x_tok, const uint16_t* gate_tok,
+                                       const uint16_t* weight, int32_t H, int32_t D, float eps,
+                                       int act, const float* ms, uint16_t* y_tok,
+                                       uint8_t* out_tok, float* scale_tok) {
+  gated_rmsnorm_row_ms(x_tok, gate_tok, weight, H, D, eps, act, ms, y_tok);
+  oracle_quant_row(y_tok, (int64_t)H * D, out_tok, scale_tok);
 }
 
 void oracle_gated_rmsnorm_quant_one(const uint16_t* x_tok, const uint16_t* gate_tok,

@@ -85,6 +85,13 @@ void oracle_gated_rmsnorm_quant_one(const uint16_t* x_tok, const uint16_t* gate_
                                     float eps, int act, uint16_t* y_tok,
                                     uint8_t* out_tok, float* scale_tok);
 
+/* The same with the mean square of each head taken from ms[H] instead of
+ * computed (a diagnostic for classifying mismatches by summation order). */
+void oracle_gated_rmsnorm_quant_one_ms(const uint16_t* x_tok, const uint16_t* gate_tok,
+                                       const uint16_t* weight, int32_t H, int32_t D, float eps,
+                                       int act, const float* ms, uint16_t* y_tok,
+                                       uint8_t* out_tok, float* scale_tok);
+
 /* ---- the steps of (A), each on its own --------------------------------- */
 /* Per-token quantisation of one bf16 row y[n]: scale = RN32(max|y| / 448),
  * codes e4m3(RN32(y / scale)); a zero row gets scale 0 and signed zeros. */

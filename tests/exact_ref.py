@@ -183,14 +183,17 @@ def act_table_exact(act: str):
 # the three operations (finite inputs)
 # ---------------------------------------------------------------------------
 
-def gated_token(x_tok, gate_tok, weight, H, D, eps: float, act: str, act_tab=None):
+def gated_token(x_tok, gate_tok, weight, H, D, eps: float, act: str, act_tab=None,
+                ms_given=None):
     """Operation (A) on one token: x_tok, gate_tok flat lists [H*D] of bf16
-    bits, weight [D].  Returns (y bits, codes, scale as Fraction)."""
+    bits, weight [D].  ms_given: None, or binary32 mean squares [H] to use in
+    place of the exact ones.  Returns (y bits, codes, scale as Fraction)."""
     epsf = rn32(Fraction(eps))
     y = []
     for h in range(H):
         xs = x_tok[h * D:(h + 1) * D]
-        r = rms_factor(mean_square(xs), epsf)
+        ms = mean_square(xs) if ms_given is None else Fraction(float(ms_given[h]))
+        r = rms_factor(ms, epsf)
         for d in range(D):
             xn = rn32(bf16_to_frac(xs[d]) * r)
             xnb = bf16_bits(xn, neg_zero=(xs[d] & 0x8000) != 0)

@@ -156,6 +156,33 @@ def test_gated_matches_exact_checker(T, H, D, act, act_tabs):
             assert codes[t].tolist() == c, (t, trial)
 
 
+@pytest.mark.parametrize("H,D,act", [(2, 32, "sigmoid"), (3, 16, "silu"), (1, 128, "sigmoid")])
+def test_gated_given_ms_matches_exact_checker(H, D, act, act_tabs):
+    """The diagnostic entry that takes each head's mean square as an input:
+    with every ms moved by -2..+2 units in the last place (one head at a
+    time, and all at once), the oracle's y, codes and scale equal the exact
+    checker's with the same ms; with the exact ms it is operation (A)."""
+    rng = random.Random(H * 31 + D + (act == "silu"))
+    xs = _rand_bf16(rng, H * D, 1.0, 0.05, 30.0)
+    gs = _rand_bf16(rng, H * D, 2.0, 0.05, 40.0)
+    w = [X.bf16_bits(X.bf16_to_frac(b) + 1) for b in _rand_bf16(rng, D, 0.3)]
+    x = np.array(xs, np.uint16).reshape(H, D)
+    g = np.array(gs, np.uint16).reshape(H, D)
+    wa = np.array(w, np.uint16)
+    ms0 = np.array([O.mean_square(x[h]) for h in range(H)], np.float32)
+    y0, c0, s0 = O.gated_rmsnorm_quant_one(x, g, wa, 1e-6, ACTS[act])
+    y1, c1, s1 = O.gated_rmsnorm_quant_one_ms(x, g, wa, 1e-6, ACTS[act], ms0)
+    assert np.array_equal(y0, y1) and np.array_equal(c0, c1) and s0 == s1
+    nudges = [(h, k) for h in range(H) for k in (-2, -1, 1, 2)] + [(None, 1)]
+    for h, k in nudges:
+        ms = ms0.copy()
+        sel = slice(None) if h is None else slice(h, h + 1)
+        ms[sel] = (ms0[sel].view(np.uint32) + np.uint32(k & 0xFFFFFFFF)).view(np.float32)
+        y, c, s = O.gated_rmsnorm_quant_one_ms(x, g, wa, 1e-6, ACTS[act], ms)
+        yx, cx, sx = X.gated_token(xs, gs, w, H, D, 1e-6, act, act_tabs[act], ms_given=ms)
+        assert y.tolist() == yx and c.tolist() == cx and Fraction(s) == sx, (h, k)
+
+
 @pytest.mark.parametrize("M,Nq,Nkv", [(1, 32, 8), (2, 64, 40), (3, 96, 64), (4, 32, 0)])
 def test_mx_matches_exact_checker(M, Nq, Nkv):
     rng = random.Random(M * 7 + Nq + Nkv)
