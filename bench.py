@@ -39,6 +39,9 @@ WORKLOAD = ("step = rmsnorm_quant_mx q[8192,1536]+kv[8192,512] -> static_head_qu
 # core for the CPU baseline, about 2 s per step for the reference arm
 CPU_SAMPLE = (4096, 8192, 16384)
 REF_SAMPLE = (512, 4096, 4096)
+# GB300's nominal HBM3e bandwidth (about 8 TB/s); the roofline fractions are
+# given against it and against the measured copy bandwidth
+NOMINAL_HBM_GBS = 8000.0
 L2_NOTE = ("inputs larger than L2: (A) 2.15 GB and (C) 2.61 GB per launch; the 55 MB of (B) "
            "is evicted by the ~5 GB the other two kernels stream between its launches")
 
@@ -177,23 +180,59 @@ def rows(inp) -> dict:
 # the oracle on the host cores (CPU baseline and reference arm)
 # ---------------------------------------------------------------------------
 
-def oracle_sample(inp, n_a, n_b, n_c):
-    """Run the oracle on the first n tokens/rows of each workload; returns
-    (seconds, algorithmic bytes of the sample, description)."""
+def oracle_sample(inp, n_a, n_b, n_c, threads: int = 1):
+    """Run the oracle on the first n tokens/rows of each workload, each
+    operation timed on its own, on `threads` host threads (row slices of the
+    same single-threaded function; 1 = as written).  Returns a dict with the
+    seconds, rows and algorithmic bytes of each operation and in total."""
     import oracle as O
     a, b, c = inp["A"], inp["B"], inp["C"]
     wl, wm, ws = a["w_"], b["w_"], c["w_"]
-    t0 = time.perf_counter()
-    O.gated_rmsnorm_quant_token(a["x"][:n_a], a["gate"][:n_a], a["w"], wl.eps, wl.act)
-    O.rmsnorm_quant_mx(b["q"][:n_b], b["wq"], b["kv"][:n_b], b["wkv"], wm.eps)
-    for k in ("q", "k", "v"):
-        O.static_head_quant(c[k][:n_c], c["d"][k])
-    dt = time.perf_counter() - t0
-    by = (n_a * wl.H * wl.D * 5 + n_b * (wm.Nq * 3 + wm.Nq // 32 + wm.Nkv * 4)
-          + n_c * ws.H * (2 * ws.Dqk + ws.Dv) * 3)
-    desc = ("first %d tokens of (A) gated_large, %d rows of (B) qkv_mx, %d tokens of (C) "
-            "static_head, single-threaded C oracle" % (n_a, n_b, n_c))
-    return dt, by, desc
+    O.lib()
+
+    def timed(fn, n):
+        t0 = time.perf_counter()
+        O.sliced(fn, n, threads=threads, min_slice=16)
+        return time.perf_counter() - t0
+
+    sec = {
+        "A": timed(lambda i, j: O.gated_rmsnorm_quant_token(a["x"][i:j], a["gate"][i:j], a["w"],
+                                                            wl.eps, wl.act), n_a),
+        "B": timed(lambda i, j: O.rmsnorm_quant_mx(b["q"][i:j], b["wq"], b["kv"][i:j], b["wkv"],
+                                                   wm.eps), n_b),
+        "C": timed(lambda i, j: [O.static_head_quant(c[k][i:j], c["d"][k]) for k in ("q", "k", "v")],
+                   n_c),
+    }
+    nrows = {"A": n_a, "B": n_b, "C": n_c}
+    by = {"A": n_a * wl.H * wl.D * 5, "B": n_b * (wm.Nq * 3 + wm.Nq // 32 + wm.Nkv * 4),
+          "C": n_c * ws.H * (2 * ws.Dqk + ws.Dv) * 3}
+    ops = {k: {"rows": nrows[k], "seconds": sec[k], "rows_per_s": nrows[k] / sec[k],
+               "GB_s": by[k] / sec[k] / 1e9} for k in sec}
+    total_s = sum(sec.values())
+    return {"threads": threads, "seconds": total_s, "bytes": sum(by.values()),
+            "GB_s": sum(by.values()) / total_s / 1e9, "ops": ops,
+            "sample": ("first %d tokens of (A) gated_large, %d rows of (B) qkv_mx, %d tokens of (C) "
+                       "static_head" % (n_a, n_b, n_c))}
+
+
+def cpu_baseline(inp) -> dict:
+    """The oracle as it stands on the host cores: single-threaded (as written)
+    and over row slices on every host thread, per operation in rows/s and
+    GB/s (rows: tokens of (A) and (C), q/kv rows of (B))."""
+    import oracle as O
+    one = oracle_sample(inp, *CPU_SAMPLE, threads=1)
+    allt = oracle_sample(inp, *CPU_SAMPLE, threads=O.host_threads())
+    names = {"A": "gated_rmsnorm_quant_token", "B": "rmsnorm_quant_mx", "C": "static_head_quant"}
+    return {"value": allt["GB_s"], "unit": UNIT, "cores": allt["threads"], "kind": "oracle",
+            "sample": allt["sample"] + "; C oracle over row slices on every host thread "
+                      "(single-threaded figures beside it)",
+            "seconds": allt["seconds"],
+            "single_thread": {"value": one["GB_s"], "unit": UNIT, "cores": 1,
+                              "seconds": one["seconds"]},
+            "per_op": {names[k]: {"rows_per_s_1_thread": one["ops"][k]["rows_per_s"],
+                                  "rows_per_s_all_threads": allt["ops"][k]["rows_per_s"],
+                                  "GB_s_1_thread": one["ops"][k]["GB_s"],
+                                  "GB_s_all_threads": allt["ops"][k]["GB_s"]} for k in names}}
 
 
 def reference_arm(args, rank: int, world: int) -> None:
@@ -206,8 +245,9 @@ def reference_arm(args, rank: int, world: int) -> None:
         oracle_sample(inp, *REF_SAMPLE)
     dts, by, desc = [], 0, ""
     for _ in range(args.steps):
-        dt, by, desc = oracle_sample(inp, *REF_SAMPLE)
-        dts.append(dt)
+        r = oracle_sample(inp, *REF_SAMPLE)
+        dts.append(r["seconds"])
+        by, desc = r["bytes"], r["sample"] + ", single-threaded C oracle"
     total = sum(dts)
     value = by * args.steps / total / 1e9
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
@@ -341,23 +381,27 @@ def ours(args, rank: int, world: int, local_rank: int) -> None:
          "ck": torch.empty(C["k"].shape, dtype=torch.uint8, device=dev),
          "cv": torch.empty(C["v"].shape, dtype=torch.uint8, device=dev)}
     stream = torch.cuda.Stream(device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def run_step(gi, oi, s, ev=None):
+        if ev:
+            ev[0].record(s)
+        B.fp8n_rmsnorm_quant_mx(gi["q"], gi["wq"], gi["kv"], gi["wkv"], wm.eps, q_out=oi["bq"],
+                                q_scale=oi["bs"], kv_out=oi["bk"], status=status, stream=s)
+        if ev:
+            ev[1].record(s)
+        B.fp8n_static_head_quant(gi["Q"], gi["K"], gi["V"], gi["dq"], gi["dk"], gi["dv"],
+                                 cu_seqlens=gi["cu"], q_out=oi["cq"], k_out=oi["ck"],
+                                 v_out=oi["cv"], status=status, stream=s)
+        if ev:
+            ev[2].record(s)
+        B.fp8n_gated_rmsnorm_quant_token(gi["x"], gi["gate"], gi["w"], wl.eps, wl.act,
+                                         out=oi["a"], scale=oi["as"], status=status, stream=s)
+        if ev:
+            ev[3].record(s)
 
     def step(ev=None):
-        if ev:
-            ev[0].record(stream)
-        B.fp8n_rmsnorm_quant_mx(g["q"], g["wq"], g["kv"], g["wkv"], wm.eps, q_out=o["bq"],
-                                q_scale=o["bs"], kv_out=o["bk"], stream=stream)
-        if ev:
-            ev[1].record(stream)
-        B.fp8n_static_head_quant(g["Q"], g["K"], g["V"], g["dq"], g["dk"], g["dv"],
-                                 cu_seqlens=g["cu"], q_out=o["cq"], k_out=o["ck"], v_out=o["cv"],
-                                 stream=stream)
-        if ev:
-            ev[2].record(stream)
-        B.fp8n_gated_rmsnorm_quant_token(g["x"], g["gate"], g["w"], wl.eps, wl.act, out=o["a"],
-                                         scale=o["as"], stream=stream)
-        if ev:
-            ev[3].record(stream)
+        run_step(g, o, stream, ev)
 
     def barrier():
         if world > 1:
@@ -398,34 +442,55 @@ def ours(args, rank: int, world: int, local_rank: int) -> None:
                               "alg_bytes": nbytes}), flush=True)
         return
 
-    # end to end through the public API with host buffers: pinned inputs copied
-    # in, the three calls, the outputs copied back, every step
+    # end to end through the public API with host buffers: every step copies
+    # its inputs in from pinned host memory, runs the three calls and copies
+    # the outputs back.  Two device buffer sets and three streams (copies in,
+    # compute, copies out) let step k's copies in overlap step k-1's compute
+    # and copies out; events order each buffer's reuse.
     h_in = {k: v.cpu().pin_memory() for k, v in g.items()}
     h_out = {k: torch.empty(v.shape, dtype=v.dtype).pin_memory() for k, v in o.items()}
     h2d = sum(v.numel() * v.element_size() for v in h_in.values())
     d2h = sum(v.numel() * v.element_size() for v in h_out.values())
+    bufs = [(g, o), ({k: torch.empty_like(v) for k, v in g.items()},
+                     {k: torch.empty_like(v) for k, v in o.items()})]
+    s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    ev_in = [torch.cuda.Event() for _ in bufs]
+    ev_comp = [torch.cuda.Event() for _ in bufs]
+    ev_out = [torch.cuda.Event() for _ in bufs]
 
-    def e2e_step():
-        for k in g:
-            g[k].copy_(h_in[k], non_blocking=True)
-        step()
-        for k in o:
-            h_out[k].copy_(o[k], non_blocking=True)
+    def e2e_run(n):
+        for k in range(n):
+            b = k % 2
+            gi, oi = bufs[b]
+            if k >= 2:
+                s_in.wait_event(ev_comp[b])   # step k-2 has read these inputs
+            with torch.cuda.stream(s_in):
+                for key in gi:
+                    gi[key].copy_(h_in[key], non_blocking=True)
+            ev_in[b].record(s_in)
+            stream.wait_event(ev_in[b])
+            if k >= 2:
+                stream.wait_event(ev_out[b])  # step k-2's outputs have left
+            run_step(gi, oi, stream)
+            ev_comp[b].record(stream)
+            s_out.wait_event(ev_comp[b])
+            with torch.cuda.stream(s_out):
+                for key in oi:
+                    h_out[key].copy_(oi[key], non_blocking=True)
+            ev_out[b].record(s_out)
 
     e2e_steps = max(3, min(args.steps, 10))
-    with torch.cuda.stream(stream):
-        for _ in range(2):
-            e2e_step()
-    stream.synchronize()
+    e2e_run(2)
+    torch.cuda.synchronize()
     barrier()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    with torch.cuda.stream(stream):
-        for _ in range(e2e_steps):
-            e2e_step()
+    s_in.wait_event(e0)
+    e2e_run(e2e_steps)
+    stream.wait_stream(s_out)
     e1.record(stream)
-    stream.synchronize()
+    torch.cuda.synchronize()
     barrier()
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
 
@@ -441,8 +506,10 @@ def ours(args, rank: int, world: int, local_rank: int) -> None:
     for k in ("A", "B", "C"):
         avg_ms = statistics.mean(per[k])
         gbs = nbytes[k] / (avg_ms * 1e-3) / 1e9
-        kernels[names[k]] = {"avg_us": 1e3 * avg_ms, "alg_bytes": nbytes[k], "GB_s": gbs,
+        kernels[names[k]] = {"avg_us": 1e3 * avg_ms, "median_us": 1e3 * statistics.median(per[k]),
+                             "alg_bytes": nbytes[k], "GB_s": gbs,
                              "frac_of_peak": gbs / pk["hbm_gbs"],
+                             "frac_of_nominal": gbs / NOMINAL_HBM_GBS,
                              "rows_per_s": nrows[k] / (avg_ms * 1e-3)}
     dom = max(kernels, key=lambda n: kernels[n]["avg_us"])
     dom_key = {v: k for k, v in names.items()}[dom]
@@ -450,7 +517,7 @@ def ours(args, rank: int, world: int, local_rank: int) -> None:
     ach = nbytes[dom_key] / (dom_ms * 1e-3) / 1e9
 
     side = side_measurements(dev, d16, inp["C"]) if world == 1 else None
-    cpu_dt, cpu_by, cpu_desc = oracle_sample(inp, *CPU_SAMPLE)
+    cpu = cpu_baseline(inp)
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
@@ -460,15 +527,17 @@ def ours(args, rank: int, world: int, local_rank: int) -> None:
             "roofline": {"bound": "hbm", "kernel": dom, "achieved": ach, "peak": pk["hbm_gbs"],
                          "unit": "GB/s", "frac": ach / pk["hbm_gbs"],
                          "peak_source": pk["source"] + " (MEASURED_PEAKS.json hbm_gbs)",
+                         "frac_of_nominal": ach / NOMINAL_HBM_GBS,
+                         "nominal_peak": NOMINAL_HBM_GBS,
                          "traffic": profiled_traffic(dom)},
             "kernels": kernels,
-            "cpu_baseline": {"value": cpu_by / cpu_dt / 1e9, "unit": UNIT, "cores": 1,
-                             "kind": "oracle", "sample": cpu_desc,
-                             "seconds": cpu_dt},
+            "status_word": int(status.item()),
+            "cpu_baseline": cpu,
             "e2e": {"value": aggregate_gbs(total_bytes, world, e2e_ms), "unit": UNIT,
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "ms_per_step": e2e_ms},
-            "gpu_launches": 3 * args.steps,  # one kernel per operation and step
+            # one kernel per operation and step in the timed region
+            "gpu_launches": 3 * args.steps,
             "clocks": clk}
     if side is not None:
         line["unfused_and_dynamic"] = side

@@ -28,7 +28,9 @@
  * Optional device status word (uint32_t*, may be NULL): kernels OR bits into
  * it and never clear it: FP8N_STATUS_BAD_DESCALE (a descale that is not finite
  * and positive was used), FP8N_STATUS_PIPELINE_TIMEOUT (a pipeline wait gave
- * up after its iteration limit; the outputs of that launch are incomplete).
+ * up after its iteration limit; the outputs of that launch are incomplete),
+ * FP8N_STATUS_BAD_SEQLENS (the sequence prefix sums given to
+ * fp8n_static_head_quant are not a valid partition of the T tokens).
  */
 #ifndef FP8NORM_H
 #define FP8NORM_H
@@ -55,6 +57,7 @@ typedef enum { FP8N_ACT_SIGMOID = 0, FP8N_ACT_SILU = 1 } fp8n_act;
 
 #define FP8N_STATUS_BAD_DESCALE 0x1u
 #define FP8N_STATUS_PIPELINE_TIMEOUT 0x2u
+#define FP8N_STATUS_BAD_SEQLENS 0x4u
 
 /* Human-readable name of a status code (static storage). */
 const char* fp8n_status_string(fp8n_status s);
@@ -220,8 +223,12 @@ fp8n_status fp8n_quant_mx(const void* y, int64_t y_stride, int64_t M, int32_t N,
  *            positive is still applied as an IEEE division and sets
  *            FP8N_STATUS_BAD_DESCALE in *status (when status is not NULL).
  * cu_seqlens: optional int32 [num_seqs + 1] device prefix sums of the packed
- *            sequences (NULL allowed).  The map is elementwise, so it is only
- *            carried for the caller's bookkeeping; T is the packed length.
+ *            sequences (NULL allowed; 4-byte aligned).  The map is elementwise,
+ *            so the codes do not depend on it; when it and status are both
+ *            given, the kernel checks on the device (no host synchronisation)
+ *            that cu_seqlens[0] == 0, that the sums never decrease and that
+ *            cu_seqlens[num_seqs] == T, and sets FP8N_STATUS_BAD_SEQLENS in
+ *            *status otherwise.
  * outputs  : e4m3, contiguous [T, H, Dqk] / [T, H, Dv].
  * Limits   : Dqk, Dv multiples of 8 in [8, 8192]; 1 <= H <= 256; fewer than
  *            2^31 16-byte chunks in Q, K and V together.
@@ -275,7 +282,10 @@ fp8n_status fp8n_dynamic_head_quant(const void* q, const void* k, const void* v,
  * (3 * 256 words, 3 KB, held by every GPU that loads the library until the
  * process exits).  The first call on each device looks up that array's
  * device address (cudaGetSymbolAddress) and caches it; make that first call
- * before any stream capture.  The call allocates nothing and zeroes the
+ * before any stream capture.  The cached address belongs to the device's
+ * primary context (the one the CUDA runtime uses): call this entry point
+ * with that context current, and not after cudaDeviceReset (which ends the
+ * context and with it the array) unless the library is loaded anew.  The call allocates nothing and zeroes the
  * array on `stream` before using it.  All calls share the one array: two
  * calls whose work overlaps on the GPU (different streams, or the same array
  * in use by an earlier call not yet finished on another stream) race and

@@ -22,6 +22,7 @@ ACT_SILU = 1
 
 STATUS_BAD_DESCALE = 0x1
 STATUS_PIPELINE_TIMEOUT = 0x2
+STATUS_BAD_SEQLENS = 0x4
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libfp8norm.so")
@@ -190,6 +191,8 @@ def fp8n_static_head_quant(q, k, v, q_descale, k_descale, v_descale, cu_seqlens=
     outs = []
     for o, d in ((q_out, Dqk), (k_out, Dqk), (v_out, Dv)):
         outs.append(o if o is not None else torch.empty((T, H, d), dtype=torch.uint8, device=q.device))
+    if cu_seqlens is not None:
+        _need(cu_seqlens, "cu_seqlens", (torch.int32,), 1)
     nseq = 0 if cu_seqlens is None else cu_seqlens.numel() - 1
     _check("fp8n_static_head_quant", lib().fp8n_static_head_quant(
         _ptr(q), _ptr(k), _ptr(v), q.stride(0), q.stride(1), v.stride(0), v.stride(1), T, H, Dqk,

@@ -45,18 +45,26 @@ def _stale(target: str, deps: list[str]) -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    """Compile and link; returns the path of the shared library."""
-    os.makedirs(OBJ, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, variant: str | None = None,
+          defines: tuple[str, ...] = ()) -> str:
+    """Compile and link; returns the path of the shared library.
+
+    variant: None builds the library (``libfp8norm.so`` next to this file);
+    a name builds a test-only copy with the given preprocessor defines into
+    ``_build/<name>/libfp8norm_<name>.so`` (e.g. the main pipeline waits
+    limited to zero iterations, to run the timeout path)."""
+    obj_dir = OBJ if variant is None else os.path.join(OBJ, variant)
+    lib_path = LIB if variant is None else os.path.join(obj_dir, "libfp8norm_%s.so" % variant)
+    os.makedirs(obj_dir, exist_ok=True)
     cc = nvcc()
     common = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2",
-                     "-I", INCLUDE, "-I", CSRC]
+                     "-I", INCLUDE, "-I", CSRC] + ["-D" + d for d in defines]
     if verbose:
         common += ["-Xptxas", "-v"]
     hdrs = _deps()
     jobs = []
     for src in sources():
-        obj = os.path.join(OBJ, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(obj_dir, os.path.basename(src)[:-3] + ".o")
         if force or _stale(obj, [src] + hdrs):
             jobs.append((src, obj))
 
@@ -73,12 +81,12 @@ def build(force: bool = False, verbose: bool = False) -> str:
         for out in ex.map(compile_one, jobs):
             if verbose and out:
                 print(out)
-    objs = [os.path.join(OBJ, os.path.basename(s)[:-3] + ".o") for s in sources()]
-    if force or jobs or _stale(LIB, objs):
-        tmp = LIB + ".tmp%d" % os.getpid()
+    objs = [os.path.join(obj_dir, os.path.basename(s)[:-3] + ".o") for s in sources()]
+    if force or jobs or _stale(lib_path, objs):
+        tmp = lib_path + ".tmp%d" % os.getpid()
         subprocess.run([cc] + ARCH + ["-shared", "-o", tmp] + objs, check=True)
-        os.replace(tmp, LIB)
-    return LIB
+        os.replace(tmp, lib_path)
+    return lib_path
 
 
 if __name__ == "__main__":

@@ -285,7 +285,8 @@ static fp8n_status check_qkv(const void* q, const void* k, const void* v, int64_
                              int64_t T, int32_t H, int32_t Dqk, int32_t Dv, void* q_out,
                              void* k_out, void* v_out, fp8n::StaticParams* p) {
   if (T < 0 || H < 1 || Dqk < 1 || Dv < 1) return FP8N_ERR_SHAPE;
-  if (Dqk % 8 || Dv % 8 || Dqk > 8192 || Dv > 8192 || H > 256) return FP8N_ERR_UNSUPPORTED;
+  if (Dqk % 8 || Dv % 8 || Dqk > 8192 || Dv > 8192 || H > fp8n::kMaxHeads)
+    return FP8N_ERR_UNSUPPORTED;
   if (qk_head_stride < Dqk || v_head_stride < Dv || qk_tok_stride < 0 || v_tok_stride < 0)
     return FP8N_ERR_SHAPE;
   // one launch addresses every chunk with 32-bit indices
@@ -323,7 +324,6 @@ fp8n_status fp8n_static_head_quant(const void* q, const void* k, const void* v,
                                    const int32_t* cu_seqlens, int32_t num_seqs, void* q_out,
                                    void* k_out, void* v_out, uint32_t* status,
                                    fp8n_stream_t stream) {
-  (void)cu_seqlens;
   if (num_seqs < 0) return FP8N_ERR_SHAPE;
   fp8n::StaticParams p = {};
   fp8n_status s = check_qkv(q, k, v, qk_tok_stride, qk_head_stride, v_tok_stride, v_head_stride,
@@ -333,9 +333,12 @@ fp8n_status fp8n_static_head_quant(const void* q, const void* k, const void* v,
   if (misaligned4(q_descale) || misaligned4(k_descale) || misaligned4(v_descale) ||
       misaligned4(status))
     return FP8N_ERR_MISALIGNED;
+  if (misaligned4(cu_seqlens)) return FP8N_ERR_MISALIGNED;
   const float* d[3] = {q_descale, k_descale, v_descale};
   for (int i = 0; i < 3; ++i) p.t[i].descale = d[i];
   p.status = status;
+  p.cu_seqlens = cu_seqlens;
+  p.num_seqs = num_seqs;
   return cuda_status(fp8n::launch_static(p, (cudaStream_t)stream));
 }
 
@@ -373,6 +376,8 @@ fp8n_status fp8n_dynamic_head_quant(const void* q, const void* k, const void* v,
 namespace {
 
 constexpr int kNoAllocMaxHeads = 256;
+// the kernels index the maxima up to 3 * H for every H the per-head calls take
+static_assert(kNoAllocMaxHeads >= fp8n::kMaxHeads, "scratch smaller than the head range");
 constexpr int kNoAllocMaxDevices = 64;
 static __device__ __align__(256) uint32_t g_dynamic_scratch[3 * kNoAllocMaxHeads];
 
@@ -429,7 +434,7 @@ fp8n_status fp8n_dynamic_head_quant_noalloc(const void* q, const void* k, const 
 fp8n_status fp8n_head_amax(const void* x, int64_t tok_stride, int64_t head_stride, int64_t T,
                            int32_t H, int32_t Dh, float* amax, fp8n_stream_t stream) {
   if (T < 0 || H < 1 || Dh < 1) return FP8N_ERR_SHAPE;
-  if (Dh % 8 || Dh > 8192 || H > 256) return FP8N_ERR_UNSUPPORTED;
+  if (Dh % 8 || Dh > 8192 || H > fp8n::kMaxHeads) return FP8N_ERR_UNSUPPORTED;
   if (head_stride < Dh || tok_stride < 0) return FP8N_ERR_SHAPE;
   if (T * H * (int64_t)Dh / 8 >= (int64_t)1 << 31) return FP8N_ERR_UNSUPPORTED;
   if (T == 0) return FP8N_OK;

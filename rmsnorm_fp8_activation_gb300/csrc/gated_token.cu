@@ -315,7 +315,7 @@ __global__ void __launch_bounds__(512) gated_token_tma(const GatedParams p, int 
   bool timeout = false;
   for (int64_t t = blockIdx.x; t < p.T; t += gridDim.x, ++it) {
     const int s = it % nstage;
-    if (!mbar_wait(smem_u32(&bars[s]), (uint32_t)(it / nstage) & 1u, kWaitLimit)) timeout = true;
+    if (!mbar_wait(smem_u32(&bars[s]), (uint32_t)(it / nstage) & 1u, kWaitLimitMain)) timeout = true;
     const uint8_t* sx = stages + (size_t)s * stage_bytes + (size_t)seg * 2;
     const uint8_t* sg = sx + row_bytes;
 
@@ -391,8 +391,12 @@ __global__ void __launch_bounds__(512) gated_token_tma(const GatedParams p, int 
       for (int m = 16; m >= 1; m >>= 1) amax = fmax_nan(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, m));
       if (lane == 0) redb[warp] = __float_as_uint(amax);
     }
-    // every thread is done with stage s and has published its warp's amax
-    if (__syncthreads_or(timeout)) break;
+    // every thread is done with stage s and has published its warp's amax; a
+    // wait that gave up in any thread stops the whole CTA (thread 0 drains)
+    if (__syncthreads_or(timeout)) {
+      timeout = true;
+      break;
+    }
     if (tid == 0) {
       const int64_t tn = t + (int64_t)nstage * gridDim.x;
       if (tn < p.T) issue(s, tn);

@@ -67,6 +67,8 @@ struct StaticParams {
   int64_t T;
   int H;
   uint32_t* status;
+  const int32_t* cu_seqlens;  // optional [num_seqs + 1], checked on the device
+  int num_seqs;
 };
 
 // Dynamic per-head quantisation: the tensors of StaticParams with descale
@@ -86,6 +88,10 @@ struct AmaxParams {
   float* amax;
 };
 
+// Largest head count of the per-head calls (per-head constants and maxima
+// live in fixed arrays of this size).
+constexpr int kMaxHeads = 256;
+
 // Number of streaming multiprocessors of the current device (cached per device).
 int sm_count();
 
@@ -97,9 +103,18 @@ cudaError_t launch_head_amax(const AmaxParams& p, cudaStream_t stream);
 cudaError_t launch_gate_act(const uint16_t* g, int64_t n, int act, uint16_t* out,
                             cudaStream_t stream);
 
-// Spin limit of every pipeline wait (iterations of mbarrier.try_wait).
+// Spin limits of the pipeline waits (iterations of mbarrier.try_wait): the
+// waits of the main loops, and the waits with which a CTA that gave up lets
+// its copies still in flight land before it exits.  A test-only build sets
+// FP8N_WAIT_LIMIT_MAIN=0, so that every main-loop wait gives up at once and
+// the timeout path (status bit, drain, early exit) runs on real copies.
+#ifndef FP8N_WAIT_LIMIT_MAIN
+#define FP8N_WAIT_LIMIT_MAIN (1u << 22)
+#endif
+constexpr uint32_t kWaitLimitMain = FP8N_WAIT_LIMIT_MAIN;
 constexpr uint32_t kWaitLimit = 1u << 22;
 constexpr uint32_t kStatusBadDescale = 0x1u;
 constexpr uint32_t kStatusTimeout = 0x2u;
+constexpr uint32_t kStatusBadSeqlens = 0x4u;
 
 }  // namespace fp8n

@@ -328,8 +328,11 @@ __global__ void __launch_bounds__(kStagedMaxWarps * 32) rmsnorm_mx_tma(const MxP
   bool timeout = false;
   for (int64_t m = gwarp; m < p.M; m += nwarps, ++it) {
     const int s = it % kSlots;
-    if (!mbar_wait(smem_u32(&bars[s]), (uint32_t)(it / kSlots) & 1u, kWaitLimit)) timeout = true;
-    if (__any_sync(0xFFFFFFFFu, timeout)) break;
+    if (!mbar_wait(smem_u32(&bars[s]), (uint32_t)(it / kSlots) & 1u, kWaitLimitMain)) timeout = true;
+    if (__any_sync(0xFFFFFFFFu, timeout)) {  // the whole warp stops (lane 0 drains)
+      timeout = true;
+      break;
+    }
     const uint4* sq = reinterpret_cast<const uint4*>(slots + (size_t)s * slot_bytes);
     const uint4* sk = reinterpret_cast<const uint4*>(slots + (size_t)s * slot_bytes + qbytes);
     sumsq2 aq, ak;

@@ -23,7 +23,6 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kUnroll = 6;
-constexpr int kMaxHeads = 256;  // largest H taken (the API rejects more)
 
 // n / d for 0 <= n < 2^31: q = (umulhi(n, m) + n) >> l with l = ceil(log2 d)
 // and m = floor(2^32 (2^l - d) / d) + 1.
@@ -50,6 +49,9 @@ struct Flat {
   int H;
   int ntensors;       // tensors walked (the amax pass of a single tensor: 1)
   uint32_t* status;
+  const int32_t* cu;  // optional sequence prefix sums [nseq + 1] (checked, not used)
+  int nseq;
+  int64_t T;
   int* amax_bits;     // dynamic variant: [3*H] per-head max |x| as float bits
   float* dout[3];     // dynamic variant: descale outputs
 };
@@ -127,6 +129,18 @@ __global__ void __launch_bounds__(kThreads) static_head_kernel(const Flat f) {
     hcs[i] = head_const(d, DYN);
   }
   if (any_bad && blockIdx.x == 0 && f.status) atomicOr(f.status, kStatusBadDescale);
+  // the packed batch's prefix sums, when given: cu[0] == 0, never decreasing,
+  // cu[nseq] == T (block 0 only; the quantisation itself is elementwise)
+  if (!DYN && blockIdx.x == 0 && f.cu && f.status) {
+    bool bad = false;
+    for (int i = threadIdx.x; i <= f.nseq; i += blockDim.x) {
+      const int32_t c = f.cu[i];
+      if (i == 0) bad |= c != 0;
+      else bad |= c < f.cu[i - 1];
+      if (i == f.nseq) bad |= (int64_t)c != f.T;
+    }
+    if (bad) atomicOr(f.status, kStatusBadSeqlens);
+  }
   __syncthreads();
 
   const uint32_t stride = gridDim.x * blockDim.x;
@@ -245,6 +259,9 @@ Flat make_flat(const StaticParams& p, uint32_t* max_chunks) {
   f.H = p.H;
   f.ntensors = 3;
   f.status = p.status;
+  f.cu = p.cu_seqlens;
+  f.nseq = p.num_seqs;
+  f.T = p.T;
   *max_chunks = acc;
   return f;
 }
@@ -317,6 +334,7 @@ cudaError_t launch_dynamic(const DynamicParams& p, cudaStream_t stream) {
   f.amax_bits = reinterpret_cast<int*>(p.amax_bits);
   for (int i = 0; i < 3; ++i) f.dout[i] = p.descale_out[i];
   f.status = nullptr;
+  f.cu = nullptr;
   cudaError_t e = cudaMemsetAsync(p.amax_bits, 0, sizeof(uint32_t) * 3 * (size_t)p.s.H, stream);
   if (e != cudaSuccess) return e;
   e = launch_amax_pass(f, chunks, stream);

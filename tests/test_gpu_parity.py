@@ -234,7 +234,7 @@ def test_mx_full_size_sampled():
 # (C)
 # ---------------------------------------------------------------------------
 
-def run_static(xs, ds, pad_tok=0):
+def run_static(xs, ds, pad_tok=0, cu=None):
     def put(a):
         if not pad_tok:
             return dev16(a)
@@ -243,9 +243,10 @@ def run_static(xs, ds, pad_tok=0):
         buf[:, :H * D] = a.reshape(T, -1)
         return dev16(buf)[:, :H * D].view(T, H, D)
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    cut = None if cu is None else torch.tensor(np.asarray(cu, np.int32), device="cuda")
     outs = B.fp8n_static_head_quant(put(xs["q"]), put(xs["k"]), put(xs["v"]),
                                     *(torch.from_numpy(ds[k]).cuda() for k in ("q", "k", "v")),
-                                    status=status)
+                                    cu_seqlens=cut, status=status)
     torch.cuda.synchronize()
     return [o.cpu().numpy() for o in outs], int(status.item())
 
@@ -263,6 +264,27 @@ def test_static_small_varlen():
     xs = {k: sw.tensor(k) for k in ("q", "k", "v")}
     assert check_static(xs, sw.descales(xs)) == 0
     assert check_static(xs, sw.descales(xs), pad_tok=64) == 0
+
+
+def test_static_cu_seqlens_checked_on_device():
+    """cu_seqlens is validated by the kernel (no host synchronisation): a
+    first sum that is not 0, a decreasing sum or a last sum other than T sets
+    FP8N_STATUS_BAD_SEQLENS; the codes do not depend on it."""
+    sw = synth.StaticHeadWorkload("t", lengths=np.array([5, 9, 300]))
+    xs = {k: sw.tensor(k) for k in ("q", "k", "v")}
+    ds = sw.descales(xs)
+    good = sw.cu_seqlens()
+    assert good.tolist() == [0, 5, 14, 314]
+    cases = {"good": (good, 0), "none": (None, 0),
+             "first_not_zero": ([1, 5, 14, 314], B.STATUS_BAD_SEQLENS),
+             "decreasing": ([0, 14, 5, 314], B.STATUS_BAD_SEQLENS),
+             "last_not_T": ([0, 5, 14, 313], B.STATUS_BAD_SEQLENS),
+             "one_seq": ([0, 314], 0), "one_seq_short": ([0, 200], B.STATUS_BAD_SEQLENS)}
+    for name, (cu, want_bits) in cases.items():
+        got, st = run_static(xs, ds, cu=cu)
+        assert st == want_bits, name
+        for i, k in enumerate(("q", "k", "v")):
+            assert np.array_equal(got[i], O.static_head_quant(xs[k], ds[k])), (name, k)
 
 
 def test_static_division_all_bf16_numerators():

@@ -6,9 +6,10 @@ pool, or a latency-critical path where cudaMalloc would synchronise the
 device): it keeps its per-head maxima in a static device array of the
 library instead of a caller workspace.  This test calls it through the C ABI
 with raw pointers and checks its descales and codes against those of the
-workspace entry point, bit for bit (the tolerance of the per-head path), on
-two calls in a row: the second call's tensors have much smaller maxima than
-the first's, so maxima left in the shared array by the first call would show.
+workspace entry point and against the oracle, bit for bit (the tolerance of
+the per-head path), on two calls in a row: the second call's tensors have
+much smaller maxima than the first's, so maxima left in the shared array by
+the first call would show.
 
 The file is named to be collected last, so that a run stopping at the first
 failure has run every other test before it; it also passes on its own in a
@@ -20,6 +21,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle as O
 import synth
 
 pytestmark = pytest.mark.gpu
@@ -68,9 +70,12 @@ def test_noalloc_matches_workspace_entry_point_twice(L):
     for xs in (first, second):
         want_d, want_c = call(L, L.fp8n_dynamic_head_quant, xs, workspace=ws)
         got_d, got_c = call(L, L.fp8n_dynamic_head_quant_noalloc, xs)
-        for i in range(3):
+        for i, n in enumerate(("q", "k", "v")):
             assert np.array_equal(got_d[i].view(np.uint32), want_d[i].view(np.uint32))
             assert np.array_equal(got_c[i], want_c[i])
+            ora_d, ora_c = O.dynamic_head_quant(xs[n])
+            assert np.array_equal(got_d[i].view(np.uint32), ora_d.view(np.uint32)), n
+            assert np.array_equal(got_c[i], ora_c), n
     assert float(got_d[0].max()) < 2.0 ** -8       # the second call's own maxima
 
 
