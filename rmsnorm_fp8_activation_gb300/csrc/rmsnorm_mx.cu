@@ -415,6 +415,288 @@ __global__ void __launch_bounds__(kStagedMaxWarps * 32) rmsnorm_mx_tma(const MxP
   }
 }
 
+// ---- rows in per-warp slots, one lane per half MX block -------------------
+//
+// The fused q/kv producer for rows of at most kRowsMaxQRounds x 512 q and
+// kRowsMaxKRounds x 256 kv elements.  One CTA per SM; warp w of the grid walks
+// rows w, w + W, w + 2W, ... (W = warps in the grid) through `nslot`
+// shared-memory slots of its own, each filled by cp.async.bulk copies on its
+// own mbarrier; the slot is refilled with the row nslot steps ahead as soon as
+// the row is done.  Every warp requests its first rows before anything else,
+// and the weights arrive by one more bulk copy on a CTA-wide mbarrier, so no
+// warp waits at a block barrier for global memory.  Shared memory fits as many
+// warps as there are row pairs to hold, so at the q/kv workload's size every
+// row of an SM is in flight from the start.
+//
+// Lane layout.  q round j: lane l owns the sixteen elements of half-block
+// hb = 32j + l (chunks 2hb and 2hb + 1), so an MX block is the lane pair
+// (l, l ^ 1): its amax is the lane's running |max| over eight bf16 pairs and
+// one xor-shuffle, and the even lane stores the E8M0 code.  The two chunks are
+// read in a rotated order (lanes with bit 2 set take the odd one first) so
+// that the eight 16-byte reads of a quarter-warp hit distinct bank groups.
+// kv round j: lane l owns chunk 32j + l.  The sums of squares of q and kv are
+// reduced over the warp together, as pairs of packed double-floats.
+constexpr int kRowsMaxQRounds = 4;
+constexpr int kRowsMaxKRounds = 4;
+constexpr int kRowsMaxWarps = 28;
+constexpr int kRowsMaxSlots = 2;
+// the weights' mbarrier, then every warp's slot mbarriers
+constexpr int kRowsHeader = 16 + kRowsMaxWarps * kRowsMaxSlots * 8;
+static_assert(kRowsHeader % 16 == 0, "weights and slots start 16-byte aligned");
+
+// Running max of |a| and |b| over bf16 pairs: the magnitude of each half is
+// the larger magnitude (NaN-propagating); its sign bit is meaningless.
+__device__ __forceinline__ uint32_t max_abs2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.NaN.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+// E4M3 code pair of y * 2^-e for a bf16 pair y, with s2 = the bf16 pattern of
+// 2^-e in both halves: each product of two bf16 values is exact in binary32
+// (mixed-precision FMA with a -0 addend, which keeps the sign of zero), then
+// one saturating nearest-even conversion.
+__device__ __forceinline__ uint32_t scaled_e4m3_pair(uint32_t y, uint32_t s2) {
+  float lo, hi;
+  asm("{\n .reg .b16 a, b, s, t;\n mov.b32 {a, b}, %2;\n mov.b32 {s, t}, %3;\n"
+      " fma.rn.f32.bf16 %0, a, s, %4;\n fma.rn.f32.bf16 %1, b, s, %4;\n}\n"
+      : "=f"(lo), "=f"(hi) : "r"(y), "r"(s2), "f"(-0.0f));
+  return e4m3x2(lo, hi);
+}
+
+// Two double-floats side by side (the q and kv sums of squares): the
+// arithmetic of df_add, lane by lane, in packed binary32.
+struct df2 {
+  f2_t h, l;
+};
+__device__ __forceinline__ df2 df2_add(df2 a, df2 b) {
+  const f2_t s = add2(a.h, b.h);
+  const f2_t bb = sub2(s, a.h);
+  const f2_t e = add2(sub2(a.h, sub2(s, bb)), sub2(b.h, bb));
+  const f2_t t = add2(e, add2(a.l, b.l));
+  const f2_t h = add2(s, t);
+  return {h, sub2(t, sub2(h, s))};
+}
+__device__ __forceinline__ df2 shfl_xor_df2(df2 v, int lane_mask) {
+  return {__shfl_xor_sync(0xFFFFFFFFu, v.h, lane_mask), __shfl_xor_sync(0xFFFFFFFFu, v.l, lane_mask)};
+}
+
+// RN32(S / n) as row_ms takes it, without a division: q = RN(S.h * RN(1/n)) is
+// within an ulp of S.h / n, so the remainder S.h - q n is exact (n <= 2^14)
+// and one correction gives the nearest binary32 of S / n except within about
+// 2^-46 S of a rounding boundary, which the uncertainty test flags.  k: the
+// additions of each running sum behind S.
+__device__ __forceinline__ float row_ms_k(df S, int n, float inv_n, bool n_pow2, int k,
+                                          bool* unsure) {
+  const float nf = (float)n;
+  float ms;
+  if (n_pow2) {
+    ms = __fmul_rn(__fadd_rn(S.h, S.l), inv_n);
+  } else {
+    const float q = __fmul_rn(S.h, inv_n);
+    const float rem = __fmaf_rn(-q, nf, S.h);
+    ms = __fadd_rn(q, __fmul_rn(__fadd_rn(rem, S.l), inv_n));
+  }
+  *unsure = ms_uncertain(S, nf, ms, __fmaf_rn(S.h, sumsq_rel_err(k, 6), nf * 0x1p-149f));
+  return ms;
+}
+
+template <int QR, int KR>
+__global__ void __launch_bounds__(kRowsMaxWarps * 32, 1) rmsnorm_mx_rows(const MxParams p, int nslot) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, wpb = blockDim.x >> 5;
+  const int64_t gwarp = (int64_t)blockIdx.x * wpb + warp;
+  const int64_t nwarps = (int64_t)gridDim.x * wpb;
+  const int qch = p.Nq / 8, kch = p.Nkv / 8, nhb = p.Nq / 16;
+  const uint32_t qbytes = 2u * (uint32_t)p.Nq, kbytes = 2u * (uint32_t)p.Nkv;
+  const uint32_t slot_bytes = qbytes + kbytes;
+  uint64_t* wbar = reinterpret_cast<uint64_t*>(smem);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + 16) + warp * kRowsMaxSlots;
+  const uint4* wq = reinterpret_cast<const uint4*>(smem + kRowsHeader);  // weights, once per CTA
+  const uint4* wk = wq + qch;
+  uint8_t* slots = smem + kRowsHeader + slot_bytes + (size_t)warp * nslot * slot_bytes;
+
+  auto issue = [&](int s, int64_t m) {
+    const uint32_t bar = smem_u32(&bars[s]);
+    const uint32_t dst = smem_u32(slots + (size_t)s * slot_bytes);
+    mbar_expect_tx(bar, slot_bytes);
+    bulk_g2s(dst, p.q + m * p.q_stride, qbytes, bar);
+    if (kbytes) bulk_g2s(dst + qbytes, p.kv + m * p.kv_stride, kbytes, bar);
+  };
+  if (lane == 0) {
+    for (int s = 0; s < nslot; ++s) mbar_init(smem_u32(&bars[s]), 1);
+    if (warp == 0) mbar_init(smem_u32(wbar), 1);
+    asm volatile("fence.mbarrier_init.release.cluster;\n fence.proxy.async.shared::cta;" ::: "memory");
+    for (int s = 0; s < nslot; ++s) {
+      const int64_t m = gwarp + s * nwarps;
+      if (m < p.M) issue(s, m);
+    }
+    if (warp == 0) {
+      const uint32_t bar = smem_u32(wbar), dst = smem_u32(smem + kRowsHeader);
+      mbar_expect_tx(bar, slot_bytes);
+      bulk_g2s(dst, p.q_weight, qbytes, bar);
+      if (kbytes) bulk_g2s(dst + qbytes, p.kv_weight, kbytes, bar);
+    }
+  }
+  __syncthreads();  // every mbarrier is initialised
+
+  const int rot = (lane >> 2) & 1;
+  const bool q_pow2 = (p.Nq & (p.Nq - 1)) == 0, k_pow2 = (p.Nkv & (p.Nkv - 1)) == 0;
+  const float inv_nq = 1.0f / (float)p.Nq, inv_nk = KR ? 1.0f / (float)p.Nkv : 0.0f;
+  bool timeout = gwarp < p.M && !mbar_wait(smem_u32(wbar), 0u, kWaitLimitMain);
+  int it = 0;
+  for (int64_t m = gwarp; m < p.M; m += nwarps, ++it) {
+    const int s = it % nslot;
+    if (!timeout && !mbar_wait(smem_u32(&bars[s]), (uint32_t)(it / nslot) & 1u, kWaitLimitMain))
+      timeout = true;
+    if (__any_sync(0xFFFFFFFFu, timeout)) {  // the whole warp stops (lane 0 drains)
+      timeout = true;
+      break;
+    }
+    const uint4* sq = reinterpret_cast<const uint4*>(slots + (size_t)s * slot_bytes);
+    const uint4* sk = sq + qch;
+    // pass 1: Sum2 of the squares (one running sum pair for q, one for kv),
+    // then both double-floats reduced over the warp together
+    sumsq2 aq, ak;
+#pragma unroll
+    for (int j = 0; j < QR; ++j) {
+      const int hb = 32 * j + lane;
+      uint4 a = make_uint4(0, 0, 0, 0), b = a, c = a;
+      if (hb < nhb) {
+        a = sq[2 * hb + rot];
+        b = sq[2 * hb + 1 - rot];
+      }
+      if (KR && j < KR && 32 * j + lane < kch) c = sk[32 * j + lane];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        aq.add_sq((&a.x)[k]);
+        aq.add_sq((&b.x)[k]);
+        if (KR && j < KR) ak.add_sq((&c.x)[k]);
+      }
+    }
+#pragma unroll
+    for (int j = QR; j < KR; ++j) {
+      uint4 c = make_uint4(0, 0, 0, 0);
+      if (32 * j + lane < kch) c = sk[32 * j + lane];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) ak.add_sq((&c.x)[k]);
+    }
+    const df vq = aq.value(), vk = ak.value();
+    df2 S = {f2(vq.h, vk.h), f2(vq.l, vk.l)};
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) S = df2_add(S, shfl_xor_df2(S, o));
+    const float2 sh = unf2(S.h), sl = unf2(S.l);
+    const df Sq = {sh.x, sl.x}, Sk = {sh.y, sl.y};
+    bool uq = false, uk = false;
+    float msq = row_ms_k(Sq, p.Nq, inv_nq, q_pow2, 8 * QR, &uq);
+    float msk = KR ? row_ms_k(Sk, p.Nkv, inv_nk, k_pow2, 4 * KR, &uk) : 0.0f;
+    if (uq) msq = row_ms_exact(sq, p.Nq, Sq, 2 * QR, msq, lane);  // rare; warp-uniform
+    if (KR && uk) msk = row_ms_exact(sk, p.Nkv, Sk, KR, msk, lane);
+    const f2_t rq = splat2(rms_factor(msq, p.eps));
+    const f2_t rk = splat2(KR ? rms_factor(msk, p.eps) : 0.0f);
+
+    // pass 2: q -> MXFP8, kv -> bf16, read from the slot again
+    uint8_t* qo = p.q_out + m * p.q_out_stride;
+    uint8_t* so = p.q_scale + m * p.q_scale_stride;
+#pragma unroll
+    for (int j = 0; j < QR; ++j) {
+      if (32 * j >= nhb) break;  // warp-uniform
+      const int hb = 32 * j + lane;
+      const bool ok = hb < nhb;
+      uint4 x0 = make_uint4(0, 0, 0, 0), x1 = x0, w0 = x0, w1 = x0;
+      if (ok) {
+        x0 = sq[2 * hb + rot];
+        x1 = sq[2 * hb + 1 - rot];
+        w0 = wq[2 * hb + rot];
+        w1 = wq[2 * hb + 1 - rot];
+      }
+      uint32_t y[8];
+      norm_chunk(x0, w0, rq, y);
+      norm_chunk(x1, w1, rq, y + 4);
+      uint32_t am = max_abs2(max_abs2(max_abs2(y[0], y[1]), max_abs2(y[2], y[3])),
+                             max_abs2(max_abs2(y[4], y[5]), max_abs2(y[6], y[7])));
+      am = max_abs2(am, __shfl_xor_sync(0xFFFFFFFFu, am, 1));
+      const uint32_t mag = am & 0x7FFF7FFFu;
+      const uint32_t code = mx_code(max(mag & 0xFFFFu, mag >> 16));
+      if (ok) {
+        if ((lane & 1) == 0) so[hb >> 1] = (uint8_t)code;
+        uint32_t o[4];
+        if (code == 0xFFu) {
+          o[0] = o[1] = o[2] = o[3] = 0x7F7F7F7Fu;
+        } else {
+          const uint32_t sb = (254u - code) << 7;  // bf16 bits of 2^-e (normal: code <= 246)
+          const uint32_t s2 = sb | (sb << 16);
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            o[k] = scaled_e4m3_pair(y[2 * k], s2) | (scaled_e4m3_pair(y[2 * k + 1], s2) << 16);
+        }
+        *reinterpret_cast<uint2*>(qo + 8 * (2 * hb + rot)) = make_uint2(o[0], o[1]);
+        *reinterpret_cast<uint2*>(qo + 8 * (2 * hb + 1 - rot)) = make_uint2(o[2], o[3]);
+      }
+    }
+    uint16_t* ko = p.kv_out + m * p.kv_out_stride;
+#pragma unroll
+    for (int j = 0; j < KR; ++j) {
+      const int c = 32 * j + lane;
+      if (c < kch) *reinterpret_cast<uint4*>(ko + 8 * c) = norm_chunk4(sk[c], wk[c], rk);
+    }
+    // the slot is free: request the row nslot steps ahead into it
+    __syncwarp();
+    if (lane == 0) {
+      const int64_t mn = m + (int64_t)nslot * nwarps;
+      if (mn < p.M) {
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        issue(s, mn);
+      }
+    }
+  }
+  if (timeout && lane == 0) {
+    if (p.status) atomicOr(p.status, kStatusTimeout);
+    for (int i = it; i < it + nslot; ++i) {
+      const int64_t mi = gwarp + (int64_t)i * nwarps;
+      if (mi < p.M) mbar_wait(smem_u32(&bars[i % nslot]), (uint32_t)(i / nslot) & 1u, kWaitLimit);
+    }
+  }
+  // the weights' copy has landed before the CTA's shared memory goes away
+  if (threadIdx.x == 0) mbar_wait(smem_u32(wbar), 0u, kWaitLimit);
+}
+
+// One CTA per SM with two row slots per warp and as many warps (up to
+// kRowsMaxWarps) as shared memory holds; a batch smaller than the grid spreads
+// its rows over more SMs with fewer warps each.
+#ifndef FP8N_ROWS_WARPS
+#define FP8N_ROWS_WARPS kRowsMaxWarps
+#endif
+template <int QR, int KR>
+cudaError_t launch_rows_v(const MxParams& p, cudaStream_t stream) {
+  auto kern = rmsnorm_mx_rows<QR, KR>;
+  const size_t slot = 2 * (size_t)(p.Nq + p.Nkv);
+  const size_t budget = 227 * 1024 - 1024 - kRowsHeader - slot;  // less the weights
+  const int nslot = kRowsMaxSlots;
+  int w = (int)(budget / ((size_t)nslot * slot));
+  if (w > FP8N_ROWS_WARPS) w = FP8N_ROWS_WARPS;
+  const int sms = sm_count();
+  const int64_t per_sm = (p.M + sms - 1) / sms;
+  if (per_sm < w) w = (int)(per_sm < 1 ? 1 : per_sm);
+  const size_t smem = kRowsHeader + slot + (size_t)w * nslot * slot;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  const int64_t need = (p.M + w - 1) / w;
+  const int grid = (int)(need < sms ? need : sms);
+  kern<<<grid, w * 32, smem, stream>>>(p, nslot);
+  return cudaGetLastError();
+}
+
+template <int QR>
+cudaError_t launch_rows_q(const MxParams& p, int kr, cudaStream_t stream) {
+  switch (kr) {
+    case 0: return launch_rows_v<QR, 0>(p, stream);
+    case 1: return launch_rows_v<QR, 1>(p, stream);
+    case 2: return launch_rows_v<QR, 2>(p, stream);
+    default: return launch_rows_v<QR, 4>(p, stream);
+  }
+}
+
 // Warps per CTA: the count (up to 32) whose CTAs pack the most warps into an
 // SM's shared memory (two row slots per warp); a row per warp-slot pair keeps
 // the slowest warp at as few rows as the SM count allows.
@@ -464,6 +746,16 @@ cudaError_t launch_variant(const MxParams& p, cudaStream_t stream) {
 // register-resident (q steps, kv steps) pair that holds the rows, else the
 // two-pass kernel.
 cudaError_t launch_mx(const MxParams& p, cudaStream_t stream) {
+  // the fused producer with rows that fit the register-resident kernel
+  const int qr = (p.Nq + 511) / 512, kr = (p.Nkv + 255) / 256;
+  if (!p.q_prenorm && p.Nq > 0 && qr <= kRowsMaxQRounds && kr <= kRowsMaxKRounds) {
+    switch (qr) {
+      case 1: return launch_rows_q<1>(p, kr, stream);
+      case 2: return launch_rows_q<2>(p, kr, stream);
+      case 3: return launch_rows_q<3>(p, kr, stream);
+      default: return launch_rows_q<4>(p, kr, stream);
+    }
+  }
   // rows of up to 3072 elements (q + kv): the staged kernel, 96 KB per CTA at most
   if (p.Nq + p.Nkv <= 3072) return launch_staged(p, stream);
   const int qs = (p.Nq / 8 + 31) / 32, ks = (p.Nkv / 8 + 31) / 32;
