@@ -74,6 +74,11 @@ def load_library(path: str) -> ctypes.CDLL:
     L.oracle_gated_rmsnorm_quant_one_ms.argtypes = [
         P, P, P, i32, i32, f32, ctypes.c_int, P, P, P, P]
     L.oracle_gated_rmsnorm_quant_one_ms.restype = None
+    L.oracle_inv_rope_row.argtypes = [P, i32, i32, i32, i32, ctypes.c_int, P, P]
+    L.oracle_inv_rope_row.restype = None
+    L.oracle_inv_rope_quant_mx.argtypes = [P, i64, i64, i32, i32, P, P, i32, i32, ctypes.c_int,
+                                           P, i64, P, i64]
+    L.oracle_inv_rope_quant_mx.restype = None
     L.oracle_rmsnorm_quant_mx.argtypes = [
         P, i64, P, i32, P, i64, P, i32, i64, f32, P, i64, P, i64, P, i64]
     L.oracle_rmsnorm_quant_mx.restype = None
@@ -273,6 +278,39 @@ def rmsnorm_quant_mx(q, q_weight, kv, kv_weight, eps: float):
         _ptr(q), Nq, _ptr(q_weight), Nq, _ptr(kv), Nkv, _ptr(kv_weight), Nkv, M, float(eps),
         _ptr(q_out), Nq, _ptr(q_scale), Nq // 32, _ptr(kv_out), Nkv)
     return q_out, q_scale, kv_out
+
+
+def inv_rope_bf16(o, positions, cos_sin, rope_off: int, rope_dim: int, interleaved: bool):
+    """The inverse-RoPE step alone: o uint16 [T, H, D] -> bf16 bits [T, H*D]."""
+    o = _c(o, np.uint16)
+    positions = _c(positions, np.int32)
+    cos_sin = _c(cos_sin, np.float32)
+    T, H, D = o.shape
+    assert cos_sin.shape[1] == rope_dim and positions.shape == (T,)
+    assert positions.min(initial=0) >= 0 and positions.max(initial=0) < cos_sin.shape[0]
+    y = np.zeros((T, H * D), dtype=np.uint16)
+    for t in range(T):
+        lib().oracle_inv_rope_row(_ptr(o[t]), H, D, int(rope_off), int(rope_dim),
+                                  int(bool(interleaved)), _ptr(cos_sin[positions[t]]), _ptr(y[t]))
+    return y
+
+
+def inv_rope_quant_mx(o, positions, cos_sin, rope_off: int, rope_dim: int, interleaved: bool):
+    """Inverse RoPE then MXFP8.  o: uint16 [T, H, D]; positions int32 [T];
+    cos_sin float32 [P, rope_dim].  Returns (codes uint8 [T, H*D], E8M0 uint8
+    [T, H*D/32])."""
+    o = _c(o, np.uint16)
+    positions = _c(positions, np.int32)
+    cos_sin = _c(cos_sin, np.float32)
+    T, H, D = o.shape
+    assert D % 32 == 0 and cos_sin.shape[1] == rope_dim and positions.shape == (T,)
+    assert positions.min(initial=0) >= 0 and positions.max(initial=0) < cos_sin.shape[0]
+    out = np.zeros((T, H * D), dtype=np.uint8)
+    scale = np.zeros((T, H * D // 32), dtype=np.uint8)
+    lib().oracle_inv_rope_quant_mx(_ptr(o), H * D, T, H, D, _ptr(positions), _ptr(cos_sin),
+                                   int(rope_off), int(rope_dim), int(bool(interleaved)),
+                                   _ptr(out), H * D, _ptr(scale), H * D // 32)
+    return out, scale
 
 
 def static_head_quant(x, descale):

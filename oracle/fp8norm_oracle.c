@@ -409,6 +409,59 @@ void oracle_quant_mx_row(const uint16_t* yq, int32_t n, uint8_t* codes, uint8_t*
 }
 
 /* ===================================================================== */
+/* Inverse RoPE, then MXFP8 (the o-projection input)                      */
+/* ===================================================================== */
+
+/* [MX] first commit message: the FP8 o-projection input comes from a fused
+ * inverse-RoPE + FP8 quantiser feeding an MX-scaled a8w8 GEMM; second commit
+ * message: the layer holds a pre-computed FP32 cos/sin cache (4096
+ * positions).  Reading: positions index rows of the cache [P, R] (cos of the
+ * R/2 pair angles, then their sin); the rotated span of each head is
+ * [rope_off, rope_off + R); pair i is (rope_off + i, rope_off + R/2 + i)
+ * (rotate-half) or (rope_off + 2i, rope_off + 2i + 1) (interleaved); the
+ * inverse rotation of a pair (x1, x2) by its angle is
+ *   y1 = x1 cos + x2 sin,  y2 = x2 cos - x1 sin,
+ * each product and sum one IEEE binary32 operation, rounded to bf16 (the
+ * model dtype); the other elements pass unchanged.  The MXFP8 quantiser of
+ * operation (B) then takes the bf16 row [H*D]. */
+void oracle_inv_rope_row(const uint16_t* o_tok, int32_t H, int32_t D, int32_t rope_off,
+                         int32_t R, int interleaved, const float* cs, uint16_t* y_tok) {
+  int32_t half = R / 2;
+  for (int64_t j = 0; j < (int64_t)H * D; ++j) y_tok[j] = o_tok[j];
+  for (int32_t h = 0; h < H; ++h) {
+    const uint16_t* x = o_tok + (int64_t)h * D;
+    uint16_t* y = y_tok + (int64_t)h * D;
+    for (int32_t i = 0; i < half; ++i) {
+      int32_t j1 = interleaved ? rope_off + 2 * i : rope_off + i;
+      int32_t j2 = interleaved ? rope_off + 2 * i + 1 : rope_off + half + i;
+      float x1 = (float)oracle_bf16_to_double(x[j1]);
+      float x2 = (float)oracle_bf16_to_double(x[j2]);
+      float c = cs[i], s = cs[half + i];
+      float a = x1 * c, b = x2 * s;
+      float y1 = a + b;
+      float d = x2 * c, e = x1 * s;
+      float y2 = d - e;
+      y[j1] = oracle_bf16_from_double((double)y1);
+      y[j2] = oracle_bf16_from_double((double)y2);
+    }
+  }
+}
+
+void oracle_inv_rope_quant_mx(const uint16_t* o, int64_t o_stride, int64_t T, int32_t H,
+                              int32_t D, const int32_t* positions, const float* cos_sin,
+                              int32_t rope_off, int32_t R, int interleaved, uint8_t* out,
+                              int64_t out_stride, uint8_t* scale, int64_t scale_stride) {
+  int64_t n = (int64_t)H * D;
+  uint16_t* y = (uint16_t*)malloc((size_t)(n > 0 ? n : 1) * sizeof(uint16_t));
+  for (int64_t t = 0; t < T; ++t) {
+    oracle_inv_rope_row(o + t * o_stride, H, D, rope_off, R, interleaved,
+                        cos_sin + (int64_t)positions[t] * R, y);
+    oracle_quant_mx_row(y, (int32_t)n, out + t * out_stride, scale + t * scale_stride);
+  }
+  free(y);
+}
+
+/* ===================================================================== */
 /* Operation (C)                                                          */
 /* ===================================================================== */
 

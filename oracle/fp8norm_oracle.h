@@ -124,6 +124,19 @@ void oracle_quant_mx_row(const uint16_t* yq, int32_t n, uint8_t* codes, uint8_t*
 /* E8M0 code of a block whose largest magnitude is the bf16 value `amax`. */
 uint8_t oracle_e8m0_code(uint16_t amax_bits);
 
+/* ---- inverse RoPE, then MXFP8 (the o-projection input) ------------------ */
+/* One token: y = o with each head's span [rope_off, rope_off + R) rotated back
+ * by the angles whose cos/sin are cs[0 .. R/2) / cs[R/2 .. R); pairs
+ * (i, i + R/2) of the span, or (2i, 2i + 1) when interleaved. */
+void oracle_inv_rope_row(const uint16_t* o_tok, int32_t H, int32_t D, int32_t rope_off,
+                         int32_t R, int interleaved, const float* cs, uint16_t* y_tok);
+/* o: [T, H, D] bf16 (token stride o_stride); positions [T] index the cache
+ * cos_sin [P, R]; out: e4m3 [T, H*D]; scale: E8M0 [T, H*D/32] row-major. */
+void oracle_inv_rope_quant_mx(const uint16_t* o, int64_t o_stride, int64_t T, int32_t H,
+                              int32_t D, const int32_t* positions, const float* cos_sin,
+                              int32_t rope_off, int32_t R, int interleaved, uint8_t* out,
+                              int64_t out_stride, uint8_t* scale, int64_t scale_stride);
+
 /* ---- operation (C): static per-head FP8 quant of packed Q/K/V ---------- */
 /* One tensor: x [T, H, Dh] bf16 with (tok_stride, head_stride) in elements,
  * descale [H] fp32; out [T, H, Dh] e4m3 contiguous. */

@@ -1,4 +1,4 @@
-"""Seeded synthetic inputs for the five workloads (no method arithmetic here).
+"""Seeded synthetic inputs of the workloads (no method arithmetic here).
 
 Every tensor is drawn from a counter-based Philox4x32-10 generator (Salmon,
 Moraes, Dror, Shaw: "Parallel random numbers: as easy as 1, 2, 3", SC'11), with
@@ -21,6 +21,9 @@ Workloads (sizes and distributions of the normalize-then-quantize path):
                 V [T, 12, 128] ~ N(0,1); descale[h] = amax_h / 448 * U(1, 1.2)
   gated_large   x, gate [65536, 64, 128] ~ N(0,1), each element x100 with
                 probability 0.01; weight 1 + 0.1 N; eps 1e-6; sigmoid
+  inv_rope_mx   o [4096, 16, 576] ~ N(0,1), RoPE on the last 64 dims of each head
+                (rotate-half), positions uniform in [0, 4096), the FP32 cos/sin
+                cache [4096, 64] of base 10000
 """
 from __future__ import annotations
 
@@ -257,6 +260,50 @@ class StaticHeadWorkload:
         return self.T * per_tok + 3 * 4 * self.H
 
 
+@dataclass
+class InvRopeWorkload:
+    """The o-projection input: attention output o [T, H, D] ~ N(0, 1) whose
+    span [rope_off, rope_off + rope_dim) of every head carries RoPE, token
+    positions uniform in [0, P), and the FP32 cos/sin cache [P, rope_dim] of
+    the angles p * base^(-2i / rope_dim) (cos of the rope_dim/2 angles, then
+    their sin), computed in double and rounded to binary32.  The cache is an
+    input of the operation, as a layer holds it."""
+    name: str
+    T: int = 4096
+    H: int = 16
+    D: int = 576
+    rope_off: int = 512
+    rope_dim: int = 64
+    interleaved: bool = False
+    P: int = 4096
+    base: float = 10000.0
+    seed: int = 0
+    stream_base: int = 0
+
+    def o(self, start_token: int = 0, n_tokens: int | None = None) -> np.ndarray:
+        if n_tokens is None:
+            n_tokens = self.T - start_token
+        row = self.H * self.D
+        v = bf16_normal(self.seed, self.stream_base + 1, n_tokens * row, start=start_token * row)
+        return v.reshape(n_tokens, self.H, self.D)
+
+    def positions(self) -> np.ndarray:
+        u = uniform(self.seed, self.stream_base + 2, 0, self.T)
+        return np.minimum(np.floor(u * self.P), self.P - 1).astype(np.int32)
+
+    def cos_sin(self) -> np.ndarray:
+        half = self.rope_dim // 2
+        theta = self.base ** (-2.0 * np.arange(half, dtype=np.float64) / self.rope_dim)
+        ang = np.arange(self.P, dtype=np.float64)[:, None] * theta[None, :]
+        return np.concatenate([np.cos(ang), np.sin(ang)], axis=1).astype(np.float32)
+
+    def algorithmic_bytes(self) -> int:
+        # read o (2 B), write e4m3 (1 B) per element and one E8M0 byte per 32;
+        # positions and the cos/sin cache once
+        n = self.T * self.H * self.D
+        return 3 * n + n // 32 + 4 * self.T + 4 * self.P * self.rope_dim
+
+
 def workloads(seed: int = 0) -> dict:
     """The five workloads, keyed by name, with independent stream ranges."""
     return {
@@ -269,4 +316,5 @@ def workloads(seed: int = 0) -> dict:
         "gated_large": GatedWorkload("gated_large", 65536, 64, 128, ACT_SIGMOID,
                                      outlier_p=0.01, outlier_scale=100.0, seed=seed,
                                      stream_base=0x500),
+        "inv_rope_mx": InvRopeWorkload("inv_rope_mx", seed=seed, stream_base=0x600),
     }

@@ -275,3 +275,56 @@ def dynamic_quant(x_bits_head):
     if d == 0:
         return d, [0x80 if b & 0x8000 else 0 for b in x_bits_head]
     return d, [e4m3_code(rn32(bf16_to_frac(b) / d), (b & 0x8000) != 0) for b in x_bits_head]
+
+
+# ---------------------------------------------------------------------------
+# inverse RoPE (binary32 products and sums, IEEE signs of zero), then MX
+# ---------------------------------------------------------------------------
+
+def _signed(v: Fraction, neg: bool):
+    """A value with the sign of zero kept: (v, negative)."""
+    return (v, (v < 0) or (v == 0 and neg))
+
+
+def _rn32_signed(x):
+    v, neg = x
+    r = rn32(v)
+    return (r, (r < 0) or (r == 0 and neg))
+
+
+def _mul32(a, b):
+    return _rn32_signed(_signed(a[0] * b[0], a[1] != b[1]))
+
+
+def _add32(a, b):
+    v = a[0] + b[0]
+    # an exact zero sum is -0 only when both addends are -0 (round to nearest)
+    return _rn32_signed(_signed(v, a[1] and b[1]))
+
+
+def _neg(a):
+    return (-a[0], not a[1])
+
+
+def _f32(x: float):
+    import math
+    return (Fraction(x), math.copysign(1.0, x) < 0)
+
+
+def inv_rope_row(o_bits, H, D, rope_off, R, interleaved, cs):
+    """One token: o_bits flat [H*D] bf16 bits; cs [R] binary32 cos then sin.
+    Returns the bf16 bits of the rotated-back row."""
+    y = list(o_bits)
+    half = R // 2
+    for h in range(H):
+        for i in range(half):
+            j1 = h * D + (rope_off + 2 * i if interleaved else rope_off + i)
+            j2 = h * D + (rope_off + 2 * i + 1 if interleaved else rope_off + half + i)
+            x1 = _signed(bf16_to_frac(o_bits[j1]), (o_bits[j1] & 0x8000) != 0)
+            x2 = _signed(bf16_to_frac(o_bits[j2]), (o_bits[j2] & 0x8000) != 0)
+            c, s = _f32(float(cs[i])), _f32(float(cs[half + i]))
+            y1 = _add32(_mul32(x1, c), _mul32(x2, s))
+            y2 = _add32(_mul32(x2, c), _neg(_mul32(x1, s)))
+            y[j1] = bf16_bits(y1[0], neg_zero=y1[1])
+            y[j2] = bf16_bits(y2[0], neg_zero=y2[1])
+    return y

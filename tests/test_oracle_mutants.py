@@ -11,6 +11,7 @@ import exact_ref as X
 import oracle as O
 import test_oracle_codecs as C
 import test_oracle_ops as P
+import test_oracle_rope as RP
 
 SRC = os.path.join(os.path.dirname(O.__file__), "fp8norm_oracle.c")
 
@@ -34,6 +35,9 @@ MUTANTS = {
                                      "out[(t * H + h) * Dh + d] = oracle_e4m3_from_float(xv / descale[H - 1 - h]);"),
     "static_multiplies": ("out[(t * H + h) * Dh + d] = oracle_e4m3_from_float(xv / descale[h]);",
                           "out[(t * H + h) * Dh + d] = oracle_e4m3_from_float(xv * (1.0f / descale[h]));"),
+    "inv_rope_forward_rotation": ("float y1 = a + b;", "float y1 = a - b;"),
+    "inv_rope_pairs_swapped": ("int32_t j1 = interleaved ? rope_off + 2 * i : rope_off + i;",
+                               "int32_t j1 = !interleaved ? rope_off + 2 * i : rope_off + i;"),
     "bf16_truncates": ("double n = rint(ldexp(a, -qexp)); /* ties to even (default rounding mode) */",
                        "double n = floor(ldexp(a, -qexp));"),
 }
@@ -54,6 +58,8 @@ def _pins(act_tabs):
         lambda: P.test_gated_matches_exact_checker(2, 1, 128, "silu", act_tabs),
         lambda: P.test_static_matches_exact_checker(3, 2, 24),
         lambda: P.test_mx_matches_exact_checker(2, 64, 40),
+        RP.test_golden_inv_rope_rows,
+        lambda: RP.test_inv_rope_matches_exact_checker(2, 64, 32, 32, True),
     ]
 
 
