@@ -271,7 +271,8 @@ def side_measurements(dev, d16, inp_c) -> dict:
     the gated_silu size fused and as gated norm -> bf16 -> per-token quant;
     (B) at the qkv_mx size fused and as RMSNorm -> bf16 -> MX quant plus the
     kv RMSNorm; the dynamic per-head quantisation of the static_head
-    workload (max pass + quantise pass)."""
+    workload (max pass + quantise pass); the inverse-RoPE + MXFP8 producer of
+    the o-projection input, fused and as its two steps."""
     import torch
     import synth
     import rmsnorm_fp8_activation_gb300 as B
@@ -280,13 +281,14 @@ def side_measurements(dev, d16, inp_c) -> dict:
     x, gt, w = d16(ws.x()), d16(ws.gate()), d16(ws.weight())
     q, kv, wq, wkv = d16(wm.q()), d16(wm.kv()), d16(wm.q_weight()), d16(wm.kv_weight())
     Q, K, V = d16(inp_c["q"]), d16(inp_c["k"]), d16(inp_c["v"])
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    flush = torch.ones(256 << 20, dtype=torch.uint8, device=dev)
+    fsum = torch.zeros((), dtype=torch.int64, device=dev)
 
     def timed(fn, n=30):
         fn()
         ts = []
         for _ in range(n):
-            flush.zero_()
+            fsum.copy_(flush.view(torch.int64).sum())  # evicts L2 with clean lines
             e0 = torch.cuda.Event(enable_timing=True)
             e1 = torch.cuda.Event(enable_timing=True)
             e0.record()
@@ -302,6 +304,14 @@ def side_measurements(dev, d16, inp_c) -> dict:
     b_unfused = timed(lambda: (B.fp8n_quant_mx(B.fp8n_rmsnorm_bf16(q, wq, wm.eps)),
                                B.fp8n_rmsnorm_bf16(kv, wkv, wm.eps)))
     dyn = timed(lambda: B.fp8n_dynamic_head_quant(Q, K, V))
+    # the o-projection input: inverse RoPE + MXFP8, fused and as its two steps
+    wr = W["inv_rope_mx"]
+    ro = d16(wr.o()).view(wr.T, wr.H, wr.D)
+    rp = torch.from_numpy(wr.positions()).to(dev)
+    rc = torch.from_numpy(wr.cos_sin()).to(dev)
+    rope_fused = timed(lambda: B.fp8n_inv_rope_quant_mx(ro, rp, rc, wr.rope_off, wr.rope_dim))
+    rope_unfused = timed(lambda: B.fp8n_quant_mx(
+        B.fp8n_inv_rope_bf16(ro, rp, rc, wr.rope_off, wr.rope_dim)))
 
     # decode-sized (A) (56 tokens x 12 heads x 128), one call replayed from a
     # CUDA graph, inputs resident (as in a decode loop): device time per call
@@ -340,7 +350,15 @@ def side_measurements(dev, d16, inp_c) -> dict:
         "dynamic_head_quant_us": dyn,
         "dynamic_head_quant_GB_s": 5 * n_c / (dyn * 1e-6) / 1e9,
         "dynamic_head_quant_bytes": "2 B/element read twice, 1 B/element written",
-        "l2": "flushed (256 MB write) before each launch",
+        "inv_rope_mx_fused_us": rope_fused, "inv_rope_mx_unfused_us": rope_unfused,
+        "inv_rope_mx_GB_s": wr.algorithmic_bytes() / (rope_fused * 1e-6) / 1e9,
+        "inv_rope_mx_frac_of_peak": wr.algorithmic_bytes() / (rope_fused * 1e-6) / 1e9
+        / peaks()["hbm_gbs"],
+        "inv_rope_mx_workload": "o [4096,16,576] bf16, rope on the last 64 dims (rotate-half), "
+                                "positions in [0,4096), fp32 cos/sin cache [4096,64]",
+        "inv_rope_mx_unfused_steps": "fp8n_inv_rope_bf16 -> fp8n_quant_mx",
+        "l2": "evicted before each launch by reading 256 MB (clean lines: no write-back "
+              "inside the timed launch)",
     }
 
 

@@ -30,7 +30,9 @@
  * and positive was used), FP8N_STATUS_PIPELINE_TIMEOUT (a pipeline wait gave
  * up after its iteration limit; the outputs of that launch are incomplete),
  * FP8N_STATUS_BAD_SEQLENS (the sequence prefix sums given to
- * fp8n_static_head_quant are not a valid partition of the T tokens).
+ * fp8n_static_head_quant are not a valid partition of the T tokens),
+ * FP8N_STATUS_BAD_POSITION (a token position outside the cos/sin cache was
+ * clamped into it by the inverse-RoPE calls).
  */
 #ifndef FP8NORM_H
 #define FP8NORM_H
@@ -55,9 +57,14 @@ typedef enum {
 
 typedef enum { FP8N_ACT_SIGMOID = 0, FP8N_ACT_SILU = 1 } fp8n_act;
 
+/* Pairing of the rotated dims in a head's RoPE span [rope_off, rope_off + R):
+ * (rope_off + i, rope_off + R/2 + i) or (rope_off + 2i, rope_off + 2i + 1). */
+typedef enum { FP8N_ROPE_HALF = 0, FP8N_ROPE_INTERLEAVED = 1 } fp8n_rope_style;
+
 #define FP8N_STATUS_BAD_DESCALE 0x1u
 #define FP8N_STATUS_PIPELINE_TIMEOUT 0x2u
 #define FP8N_STATUS_BAD_SEQLENS 0x4u
+#define FP8N_STATUS_BAD_POSITION 0x8u
 
 /* Human-readable name of a status code (static storage). */
 const char* fp8n_status_string(fp8n_status s);
@@ -204,6 +211,55 @@ fp8n_status fp8n_rmsnorm_bf16(const void* x, int64_t x_stride, const void* weigh
 fp8n_status fp8n_quant_mx(const void* y, int64_t y_stride, int64_t M, int32_t N, void* out,
                           int64_t out_stride, uint8_t* scale, int64_t scale_stride,
                           uint32_t* status, fp8n_stream_t stream);
+
+/*
+ * Inverse RoPE of the o-projection input, then MXFP8.
+ *
+ * Source: "[ROCm][Perf] FP8 o-projection for DeepSeek-V4.1-Flash MLA on AMD
+ * MI355X" (vLLM PR 57081): first commit message (a fused inverse-RoPE + FP8
+ * quantiser feeds the MX-scaled a8w8 o-projection GEMM) and second commit
+ * message (the layer holds a pre-computed FP32 cos/sin cache of 4096
+ * positions).  The pages give neither the rotation convention nor the cache
+ * layout; both are arguments here.
+ *
+ * Per token t, with cache row cs = cos_sin[positions[t]] (cos of the R/2
+ * pair angles, then their sin), every head's span [rope_off, rope_off + R)
+ * is rotated back pair by pair (pair i as fp8n_rope_style says):
+ *   y1 = bf16(RN32(RN32(x1 * cs[i]) + RN32(x2 * cs[R/2 + i])))
+ *   y2 = bf16(RN32(RN32(x2 * cs[i]) - RN32(x1 * cs[R/2 + i])))
+ * other elements pass unchanged; the bf16 row [H*D] is then quantised as the
+ * q part of fp8n_rmsnorm_quant_mx: per 32 consecutive elements
+ *   e = clamp(floor(log2 max|y|) - 8, -127, 127), scale = e + 127,
+ *   out = e4m3(y * 2^-e).
+ * fp8n_quant_mx(fp8n_inv_rope_bf16(...)) equals this call bit for bit.
+ *
+ * o        : bf16 [T, H, D], heads contiguous, token stride o_stride
+ *            (elements, multiple of 8, >= H*D).
+ * positions: int32 [T] device, each in [0, num_positions); a position
+ *            outside is clamped into the cache and sets
+ *            FP8N_STATUS_BAD_POSITION (when status is not NULL).
+ * cos_sin  : fp32 [num_positions, rope_dim] device, 16-byte aligned.
+ * out      : e4m3 [T, H*D], token stride out_stride (bytes, multiple of 16).
+ * scale    : E8M0 uint8 [T, H*D/32] row-major, token stride scale_stride.
+ * Limits   : D a multiple of 32 in [32, 8192]; rope_off a multiple of 8;
+ *            rope_dim a multiple of 16 (0: no rotation, only the MXFP8);
+ *            rope_off + rope_dim <= D; fewer than 2^31 MX blocks in all.
+ */
+fp8n_status fp8n_inv_rope_quant_mx(const void* o, int64_t o_stride, int64_t T, int32_t H,
+                                   int32_t D, const int32_t* positions, const float* cos_sin,
+                                   int32_t num_positions, int32_t rope_off, int32_t rope_dim,
+                                   fp8n_rope_style style, void* out, int64_t out_stride,
+                                   uint8_t* scale, int64_t scale_stride, uint32_t* status,
+                                   fp8n_stream_t stream);
+
+/* The inverse-RoPE step alone: y[t, :] = the rotated bf16 row above.
+ * y: bf16 [T, H*D], token stride y_stride (elements, multiple of 8).  Other
+ * arguments and limits: as fp8n_inv_rope_quant_mx. */
+fp8n_status fp8n_inv_rope_bf16(const void* o, int64_t o_stride, int64_t T, int32_t H, int32_t D,
+                               const int32_t* positions, const float* cos_sin,
+                               int32_t num_positions, int32_t rope_off, int32_t rope_dim,
+                               fp8n_rope_style style, void* y, int64_t y_stride, uint32_t* status,
+                               fp8n_stream_t stream);
 
 /*
  * (C) Static per-head FP8 quantisation of packed variable-length Q, K, V.

@@ -23,6 +23,9 @@ ACT_SILU = 1
 STATUS_BAD_DESCALE = 0x1
 STATUS_PIPELINE_TIMEOUT = 0x2
 STATUS_BAD_SEQLENS = 0x4
+STATUS_BAD_POSITION = 0x8
+ROPE_HALF = 0
+ROPE_INTERLEAVED = 1
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libfp8norm.so")
@@ -78,9 +81,13 @@ def lib() -> ctypes.CDLL:
         L.fp8n_dynamic_head_quant_noalloc.argtypes = [
             P, P, P, i64, i64, i64, i64, i64, i32, i32, i32, P, P, P, P, P, P, P]
         L.fp8n_dynamic_head_quant_noalloc.restype = ctypes.c_int
+        L.fp8n_inv_rope_quant_mx.argtypes = [
+            P, i64, i64, i32, i32, P, P, i32, i32, i32, ctypes.c_int, P, i64, P, i64, P, P]
+        L.fp8n_inv_rope_bf16.argtypes = [
+            P, i64, i64, i32, i32, P, P, i32, i32, i32, ctypes.c_int, P, i64, P, P]
         for name in ("fp8n_gated_rmsnorm_bf16", "fp8n_quant_token", "fp8n_gated_quant_token",
                      "fp8n_rmsnorm_bf16", "fp8n_quant_mx", "fp8n_dynamic_head_quant",
-                     "fp8n_head_amax"):
+                     "fp8n_head_amax", "fp8n_inv_rope_quant_mx", "fp8n_inv_rope_bf16"):
             getattr(L, name).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -199,6 +206,51 @@ def fp8n_static_head_quant(q, k, v, q_descale, k_descale, v_descale, cu_seqlens=
         Dv, _ptr(q_descale), _ptr(k_descale), _ptr(v_descale), _ptr(cu_seqlens), nseq,
         _ptr(outs[0]), _ptr(outs[1]), _ptr(outs[2]), _ptr(status), _stream(stream)))
     return tuple(outs)
+
+
+def _rope_args(o, positions, cos_sin, rope_dim):
+    _need(o, "o", _BF16, 3)
+    T, H, D = o.shape
+    if o.stride(1) != D:
+        raise ValueError("o: heads must be contiguous inside a token")
+    if rope_dim > 0:
+        _need(positions, "positions", (torch.int32,), 1)
+        _need(cos_sin, "cos_sin", (torch.float32,), 2)
+        if positions.shape[0] != T or cos_sin.shape[1] != rope_dim or not cos_sin.is_contiguous():
+            raise ValueError("positions must be [T] and cos_sin a contiguous [P, rope_dim]")
+    P = 0 if cos_sin is None else cos_sin.shape[0]
+    return T, H, D, P
+
+
+def fp8n_inv_rope_quant_mx(o, positions, cos_sin, rope_off: int, rope_dim: int,
+                           style: int = ROPE_HALF, out=None, scale=None, status=None, stream=None):
+    """Inverse RoPE then MXFP8.  o: [T, H, D] bf16; positions int32 [T];
+    cos_sin fp32 [P, rope_dim].  Returns (out uint8 [T, H*D], scale uint8 E8M0
+    [T, H*D/32])."""
+    T, H, D, P = _rope_args(o, positions, cos_sin, rope_dim)
+    if out is None:
+        out = torch.empty((T, H * D), dtype=torch.uint8, device=o.device)
+    if scale is None:
+        scale = torch.empty((T, H * D // 32), dtype=torch.uint8, device=o.device)
+    _need(out, "out", _U8, 2)
+    _check("fp8n_inv_rope_quant_mx", lib().fp8n_inv_rope_quant_mx(
+        _ptr(o), o.stride(0), T, H, D, _ptr(positions), _ptr(cos_sin), P, rope_off, rope_dim,
+        style, _ptr(out), out.stride(0), _ptr(scale), scale.stride(0), _ptr(status),
+        _stream(stream)))
+    return out, scale
+
+
+def fp8n_inv_rope_bf16(o, positions, cos_sin, rope_off: int, rope_dim: int,
+                       style: int = ROPE_HALF, y=None, status=None, stream=None):
+    """The inverse-RoPE step alone: bf16 [T, H*D]."""
+    T, H, D, P = _rope_args(o, positions, cos_sin, rope_dim)
+    if y is None:
+        y = torch.empty((T, H * D), dtype=torch.bfloat16, device=o.device)
+    _need(y, "y", _BF16, 2)
+    _check("fp8n_inv_rope_bf16", lib().fp8n_inv_rope_bf16(
+        _ptr(o), o.stride(0), T, H, D, _ptr(positions), _ptr(cos_sin), P, rope_off, rope_dim,
+        style, _ptr(y), y.stride(0), _ptr(status), _stream(stream)))
+    return y
 
 
 def fp8n_gate_act_bf16(g, act: int = ACT_SIGMOID, out=None, stream=None):

@@ -452,6 +452,80 @@ fp8n_status fp8n_head_amax(const void* x, int64_t tok_stride, int64_t head_strid
   return cuda_status(fp8n::launch_head_amax(p, (cudaStream_t)stream));
 }
 
+// Shared validation of the inverse-RoPE calls; fills the input side of p.
+static fp8n_status check_rope(const void* o, int64_t o_stride, int64_t T, int32_t H, int32_t D,
+                              const int32_t* positions, const float* cos_sin,
+                              int32_t num_positions, int32_t rope_off, int32_t rope_dim,
+                              fp8n_rope_style style, uint32_t* status, fp8n::RopeParams* p) {
+  if (T < 0 || H < 1 || D < 1 || rope_off < 0 || rope_dim < 0) return FP8N_ERR_SHAPE;
+  if (style != FP8N_ROPE_HALF && style != FP8N_ROPE_INTERLEAVED) return FP8N_ERR_UNSUPPORTED;
+  if (D % 32 || D > 8192 || rope_off % 8 || rope_dim % 16 || rope_off + rope_dim > D)
+    return FP8N_ERR_UNSUPPORTED;
+  // one launch addresses every MX block with 32-bit indices
+  if (T * H * (int64_t)(D / 32) >= (int64_t)1 << 31) return FP8N_ERR_UNSUPPORTED;
+  if (o_stride < (int64_t)H * D) return FP8N_ERR_SHAPE;
+  if (rope_dim > 0 && num_positions < 1) return FP8N_ERR_SHAPE;
+  if (T == 0) return FP8N_OK;
+  if (!o || (rope_dim > 0 && (!positions || !cos_sin))) return FP8N_ERR_NULL;
+  if (!aligned16(o) || o_stride % 8 || (rope_dim > 0 && (!aligned16(cos_sin) || misaligned4(positions))) ||
+      misaligned4(status))
+    return FP8N_ERR_MISALIGNED;
+  p->o = (const uint16_t*)o;
+  p->o_stride = o_stride;
+  p->T = T;
+  p->H = H;
+  p->D = D;
+  p->positions = positions;
+  p->cos_sin = cos_sin;
+  p->P = num_positions;
+  p->rope_off = rope_off;
+  p->R = rope_dim;
+  p->interleaved = style == FP8N_ROPE_INTERLEAVED;
+  p->status = status;
+  return FP8N_OK;
+}
+
+fp8n_status fp8n_inv_rope_quant_mx(const void* o, int64_t o_stride, int64_t T, int32_t H,
+                                   int32_t D, const int32_t* positions, const float* cos_sin,
+                                   int32_t num_positions, int32_t rope_off, int32_t rope_dim,
+                                   fp8n_rope_style style, void* out, int64_t out_stride,
+                                   uint8_t* scale, int64_t scale_stride, uint32_t* status,
+                                   fp8n_stream_t stream) {
+  fp8n::RopeParams p = {};
+  fp8n_status s = check_rope(o, o_stride, T, H, D, positions, cos_sin, num_positions, rope_off,
+                             rope_dim, style, status, &p);
+  if (s != FP8N_OK) return s;
+  if (out_stride < (int64_t)H * D || scale_stride < (int64_t)H * (D / 32)) return FP8N_ERR_SHAPE;
+  if (T == 0) return FP8N_OK;
+  if (!out || !scale) return FP8N_ERR_NULL;
+  if (!aligned16(out) || out_stride % 16) return FP8N_ERR_MISALIGNED;
+  p.quant = 1;
+  p.out = (uint8_t*)out;
+  p.out_stride = out_stride;
+  p.scale = scale;
+  p.scale_stride = scale_stride;
+  return cuda_status(fp8n::launch_inv_rope(p, (cudaStream_t)stream));
+}
+
+fp8n_status fp8n_inv_rope_bf16(const void* o, int64_t o_stride, int64_t T, int32_t H, int32_t D,
+                               const int32_t* positions, const float* cos_sin,
+                               int32_t num_positions, int32_t rope_off, int32_t rope_dim,
+                               fp8n_rope_style style, void* y, int64_t y_stride, uint32_t* status,
+                               fp8n_stream_t stream) {
+  fp8n::RopeParams p = {};
+  fp8n_status s = check_rope(o, o_stride, T, H, D, positions, cos_sin, num_positions, rope_off,
+                             rope_dim, style, status, &p);
+  if (s != FP8N_OK) return s;
+  if (y_stride < (int64_t)H * D) return FP8N_ERR_SHAPE;
+  if (T == 0) return FP8N_OK;
+  if (!y) return FP8N_ERR_NULL;
+  if (!aligned16(y) || y_stride % 8) return FP8N_ERR_MISALIGNED;
+  p.quant = 0;
+  p.y_out = (uint16_t*)y;
+  p.y_stride = y_stride;
+  return cuda_status(fp8n::launch_inv_rope(p, (cudaStream_t)stream));
+}
+
 fp8n_status fp8n_gate_act_bf16(const void* g, int64_t n, fp8n_act act, void* out,
                                fp8n_stream_t stream) {
   if (n < 0) return FP8N_ERR_SHAPE;

@@ -88,6 +88,27 @@ struct AmaxParams {
   float* amax;
 };
 
+// Inverse RoPE of the o-projection input, then MXFP8 (or, without the
+// quantisation, the rotated bf16 row).
+struct RopeParams {
+  const uint16_t* o;  // [T, H, D] bf16, token stride o_stride
+  int64_t o_stride;
+  int64_t T;
+  int H, D;
+  const int32_t* positions;  // [T]
+  const float* cos_sin;      // [P, R]: cos of the R/2 pair angles, then their sin
+  int P, rope_off, R;
+  int interleaved;  // pairs (2i, 2i+1) of the span instead of (i, i + R/2)
+  int quant;        // 1: codes and E8M0 scales; 0: the bf16 rows y_out
+  uint8_t* out;     // [T, H*D] e4m3
+  int64_t out_stride;
+  uint8_t* scale;   // [T, H*D/32] E8M0
+  int64_t scale_stride;
+  uint16_t* y_out;  // [T, H*D] bf16
+  int64_t y_stride;
+  uint32_t* status;
+};
+
 // Largest head count of the per-head calls (per-head constants and maxima
 // live in fixed arrays of this size).
 constexpr int kMaxHeads = 256;
@@ -100,6 +121,7 @@ cudaError_t launch_mx(const MxParams& p, cudaStream_t stream);
 cudaError_t launch_static(const StaticParams& p, cudaStream_t stream);
 cudaError_t launch_dynamic(const DynamicParams& p, cudaStream_t stream);
 cudaError_t launch_head_amax(const AmaxParams& p, cudaStream_t stream);
+cudaError_t launch_inv_rope(const RopeParams& p, cudaStream_t stream);
 cudaError_t launch_gate_act(const uint16_t* g, int64_t n, int act, uint16_t* out,
                             cudaStream_t stream);
 
@@ -116,5 +138,6 @@ constexpr uint32_t kWaitLimit = 1u << 22;
 constexpr uint32_t kStatusBadDescale = 0x1u;
 constexpr uint32_t kStatusTimeout = 0x2u;
 constexpr uint32_t kStatusBadSeqlens = 0x4u;
+constexpr uint32_t kStatusBadPosition = 0x8u;
 
 }  // namespace fp8n

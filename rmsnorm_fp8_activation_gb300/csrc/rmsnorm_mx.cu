@@ -265,14 +265,6 @@ __device__ __forceinline__ uint32_t block_amax_bits(const uint32_t y[4]) {
   return __float_as_uint(fmax_nan(bf16_lo(m), bf16_hi(m))) >> 16;
 }
 
-// E8M0 code of a block from its amax bits A: floor(log2 A) is the exponent
-// field minus 127 for a normal A, so code = e + 127 = field - 8, clamped at 0
-// (which also covers zero and subnormal blocks); 0xFF for NaN or infinity.
-__device__ __forceinline__ uint32_t mx_code(uint32_t A) {
-  const uint32_t ef = A >> 7;
-  return ef == 0xFFu ? 0xFFu : (ef > 8u ? ef - 8u : 0u);
-}
-
 // Staged variant for rows that fit two per-warp slots: each warp owns two
 // shared-memory slots (q row then kv row) filled by cp.async.bulk on its own
 // mbarriers, and starts the copy of its next-but-one row as soon as a slot is
@@ -443,26 +435,6 @@ constexpr int kRowsMaxSlots = 2;
 // the weights' mbarrier, then every warp's slot mbarriers
 constexpr int kRowsHeader = 16 + kRowsMaxWarps * kRowsMaxSlots * 8;
 static_assert(kRowsHeader % 16 == 0, "weights and slots start 16-byte aligned");
-
-// Running max of |a| and |b| over bf16 pairs: the magnitude of each half is
-// the larger magnitude (NaN-propagating); its sign bit is meaningless.
-__device__ __forceinline__ uint32_t max_abs2(uint32_t a, uint32_t b) {
-  uint32_t d;
-  asm("max.NaN.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
-  return d;
-}
-
-// E4M3 code pair of y * 2^-e for a bf16 pair y, with s2 = the bf16 pattern of
-// 2^-e in both halves: each product of two bf16 values is exact in binary32
-// (mixed-precision FMA with a -0 addend, which keeps the sign of zero), then
-// one saturating nearest-even conversion.
-__device__ __forceinline__ uint32_t scaled_e4m3_pair(uint32_t y, uint32_t s2) {
-  float lo, hi;
-  asm("{\n .reg .b16 a, b, s, t;\n mov.b32 {a, b}, %2;\n mov.b32 {s, t}, %3;\n"
-      " fma.rn.f32.bf16 %0, a, s, %4;\n fma.rn.f32.bf16 %1, b, s, %4;\n}\n"
-      : "=f"(lo), "=f"(hi) : "r"(y), "r"(s2), "f"(-0.0f));
-  return e4m3x2(lo, hi);
-}
 
 // Two double-floats side by side (the q and kv sums of squares): the
 // arithmetic of df_add, lane by lane, in packed binary32.

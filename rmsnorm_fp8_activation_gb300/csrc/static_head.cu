@@ -24,23 +24,6 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kUnroll = 6;
 
-// n / d for 0 <= n < 2^31: q = (umulhi(n, m) + n) >> l with l = ceil(log2 d)
-// and m = floor(2^32 (2^l - d) / d) + 1.
-struct FastDiv {
-  uint32_t d, m, l;
-};
-
-FastDiv make_fastdiv(uint32_t d) {
-  uint32_t l = 0;
-  while ((1ull << l) < d) ++l;
-  const uint64_t m = ((1ull << 32) * ((1ull << l) - d)) / d + 1;
-  return {d, (uint32_t)m, l};
-}
-
-__device__ __forceinline__ uint32_t fdiv(uint32_t n, const FastDiv& f) {
-  return (__umulhi(n, f.m) + n) >> f.l;
-}
-
 struct Flat {
   StaticTensor t[3];
   FastDiv cpr[3];     // chunks per (token, head) row

@@ -187,3 +187,33 @@ def test_dynamic_and_amax_validation(L):
     assert L.fp8n_head_amax(P16, 2304, 100, 10, 12, 192, P16, None) == SHAPE
     assert L.fp8n_head_amax(P16, 2304, 192, 10, 12, 192, None, None) == NULL
     assert L.fp8n_head_amax(P16 + 8, 2304, 192, 10, 12, 192, P16, None) == MISALIGNED
+
+
+def test_inv_rope_validation(L):
+    def rope(fn="q", **kw):
+        a = dict(o=P16, os=9216, T=10, H=16, D=576, pos=P16, cs=P16, P=4096, off=512, R=64,
+                 style=0, out=P16, ost=9216, sc=P16, sst=288, st=None)
+        a.update(kw)
+        if fn == "q":
+            return L.fp8n_inv_rope_quant_mx(a["o"], a["os"], a["T"], a["H"], a["D"], a["pos"],
+                                            a["cs"], a["P"], a["off"], a["R"], a["style"],
+                                            a["out"], a["ost"], a["sc"], a["sst"], a["st"], None)
+        return L.fp8n_inv_rope_bf16(a["o"], a["os"], a["T"], a["H"], a["D"], a["pos"], a["cs"],
+                                    a["P"], a["off"], a["R"], a["style"], a["out"], a["ost"],
+                                    a["st"], None)
+    assert rope(T=0) == OK and rope("y", T=0) == OK
+    assert rope(D=560) == UNSUPPORTED                  # D not a multiple of 32
+    assert rope(off=516) == UNSUPPORTED                # span start not on a chunk
+    assert rope(R=56) == UNSUPPORTED                   # span not whole chunk pairs
+    assert rope(off=544, R=64) == UNSUPPORTED          # span past the head
+    assert rope(style=2) == UNSUPPORTED
+    assert rope(T=1 << 30) == UNSUPPORTED              # beyond 2^31 MX blocks
+    assert rope(os=9000) == SHAPE
+    assert rope(sst=287) == SHAPE
+    assert rope(P=0) == SHAPE
+    assert rope(pos=None) == NULL and rope(cs=None) == NULL and rope(sc=None) == NULL
+    assert rope(cs=P16 + 4) == MISALIGNED
+    assert rope(ost=9224) == MISALIGNED                # code rows of 16-byte multiples
+    assert rope(os=9220) == MISALIGNED
+    assert rope("y", out=P16 + 8) == MISALIGNED
+    assert rope("y", ost=9000) == SHAPE

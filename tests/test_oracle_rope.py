@@ -105,3 +105,34 @@ def test_inv_rope_workload_inputs():
     assert cs.shape == (w.P, w.rope_dim) and cs.dtype == np.float32
     assert np.all(cs[0, :32] == 1.0) and np.all(cs[0, 32:] == 0.0)
     assert np.allclose(cs[:, :32] ** 2 + cs[:, 32:] ** 2, 1.0, atol=1e-6)
+
+
+# Two rotations from the o-projection workload whose sum lies so close to a
+# bf16 rounding boundary that rounding x1*c + x2*s once (a fused multiply-add)
+# gives the other bf16 neighbour than rounding the product and the sum apart:
+# (x1, x2, cos, sin) as bf16 / binary32 bit patterns, and the two results.
+CONTRACTION_CASES = [
+    (0x3E8E, 0xBF05, 0x3F73BDEA, 0x3E9C8953, 0x3DD8, 0x3DD7),
+    (0x3D8B, 0x3FB1, 0xBF7FB319, 0x3D465E5E, 0xBA58, 0xBA57),
+]
+
+
+def contraction_row():
+    """One token, one head of 32 with the two cases as pairs 0 and 1."""
+    o = np.zeros((1, 1, 32), np.uint16)
+    cs = np.zeros((1, 32), np.float32)
+    cs[0, :16] = 1.0
+    for i, (x1, x2, c, s, _, _) in enumerate(CONTRACTION_CASES):
+        o[0, 0, i], o[0, 0, 16 + i] = x1, x2
+        cs[0, i] = np.array([c], np.uint32).view(np.float32)[0]
+        cs[0, 16 + i] = np.array([s], np.uint32).view(np.float32)[0]
+    return o, cs
+
+
+def test_inv_rope_rounds_product_and_sum_apart():
+    o, cs = contraction_row()
+    y = O.inv_rope_bf16(o, np.zeros(1, np.int32), cs, 0, 32, False)
+    want = X.inv_rope_row(o.reshape(-1).tolist(), 1, 32, 0, 32, False, cs[0].tolist())
+    assert y[0].tolist() == want
+    for i, (_, _, _, _, apart, fused) in enumerate(CONTRACTION_CASES):
+        assert y[0, i] == apart and apart != fused
