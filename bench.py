@@ -339,6 +339,27 @@ def side_measurements(dev, d16, inp_c) -> dict:
     g1.record()
     torch.cuda.synchronize()
     small_us = 1e3 * g0.elapsed_time(g1) / reps
+    # the same call as one node among 20 in a graph (as in a decode step's
+    # graph): the graph's own launch is spread over its nodes
+    nodes = 20
+    graph20 = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph20, stream=cs):
+        for _ in range(nodes):
+            B.fp8n_gated_rmsnorm_quant_token(xd, gd, wtd, wd.eps, wd.act, out=od, scale=sd)
+    for _ in range(5):
+        graph20.replay()
+    torch.cuda.synchronize()
+    g0.record()
+    for _ in range(20):
+        graph20.replay()
+    g1.record()
+    torch.cuda.synchronize()
+    small_node_us = 1e3 * g0.elapsed_time(g1) / (20 * nodes)
+    # a plain device copy of as many bytes as the q/kv producer moves (27.5 MB
+    # read, 27.5 MB written): what one stream of this size takes here
+    cp_src = torch.empty(wm.algorithmic_bytes() // 4, dtype=torch.int16, device=dev)
+    cp_dst = torch.empty_like(cp_src)
+    copy_us = timed(lambda: cp_dst.copy_(cp_src))
     n_c = Q.numel() + K.numel() + V.numel()
     return {
         "gated_silu_fused_us": a_fused, "gated_silu_unfused_us": a_unfused,
@@ -347,6 +368,11 @@ def side_measurements(dev, d16, inp_c) -> dict:
         "qkv_mx_unfused_steps": "fp8n_rmsnorm_bf16(q) -> fp8n_quant_mx; fp8n_rmsnorm_bf16(kv)",
         "gated_small_graph_us": small_us,
         "gated_small_graph_note": "56 x 12 x 128 sigmoid, one call per graph replay, inputs resident",
+        "gated_small_graph_node_us": small_node_us,
+        "gated_small_graph_node_note": "the same call as one of 20 nodes of a graph (per node)",
+        "copy_55MB_us": copy_us,
+        "copy_55MB_note": "torch device copy of the q/kv producer's algorithmic bytes (half read, "
+                          "half written): a plain stream of this size, for context",
         "dynamic_head_quant_us": dyn,
         "dynamic_head_quant_GB_s": 5 * n_c / (dyn * 1e-6) / 1e9,
         "dynamic_head_quant_bytes": "2 B/element read twice, 1 B/element written",

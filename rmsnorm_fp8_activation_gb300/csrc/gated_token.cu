@@ -284,11 +284,18 @@ __global__ void __launch_bounds__(512) gated_token_tma(const GatedParams p, int 
     bulk_g2s(dst, p.x + t * p.x_stride, row_bytes, bar);
     if (M::gate) bulk_g2s(dst + row_bytes, p.gate + t * p.gate_stride, row_bytes, bar);
   };
-  // the first rows are requested before anything else, so that their copies
-  // overlap the weight load and the table fill
+  // programmatic dependent launch: the next kernel of the stream may start its
+  // launch now (it waits for this one to finish before it touches memory), and
+  // this one touches global memory only once the previous kernel is done
+  pdl_launch_dependents();
   if (tid == 0) {
     for (int s = 0; s < nstage; ++s) mbar_init(smem_u32(&bars[s]), 1);
     asm volatile("fence.mbarrier_init.release.cluster;\n fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  pdl_wait();
+  // the first rows are requested before anything else, so that their copies
+  // overlap the weight load and the table fill
+  if (tid == 0) {
     for (int s = 0; s < nstage; ++s) {
       int64_t t = blockIdx.x + (int64_t)s * gridDim.x;
       if (t < p.T) issue(s, t);
@@ -551,6 +558,8 @@ __device__ __forceinline__ void generic_token(const GatedParams& p, int64_t t, u
 template <int MODE, int ACT>
 __global__ void __launch_bounds__(256) gated_token_generic(const GatedParams p) {
   extern __shared__ __align__(1024) uint8_t smem[];
+  pdl_launch_dependents();  // programmatic dependent launch (see launch_pdl)
+  pdl_wait();
   for (int64_t t = blockIdx.x; t < p.T; t += gridDim.x) generic_token<MODE, ACT>(p, t, smem);
 }
 
@@ -578,8 +587,7 @@ cudaError_t launch_tma_v(const GatedParams& p, cudaStream_t stream) {
   if (per_sm < 1) per_sm = 1;
   const int64_t want = (int64_t)sm_count() * per_sm;
   const int grid = (int)(p.T < want ? p.T : want);
-  kern<<<grid, block, smem, stream>>>(p, nstage);
-  return cudaGetLastError();
+  return launch_pdl(kern, grid, block, smem, stream, p, nstage);
 }
 
 template <int MODE, int ACT, int CPT, int TPH>
@@ -612,8 +620,7 @@ cudaError_t launch_generic(const GatedParams& p, cudaStream_t stream) {
   if (per_sm < 1) per_sm = 1;
   const int64_t want = (int64_t)sm_count() * per_sm;
   const int grid = (int)(p.T < want ? p.T : want);
-  kern<<<grid, 256, smem, stream>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(kern, grid, 256, smem, stream, p);
 }
 
 template <int MODE, int ACT>

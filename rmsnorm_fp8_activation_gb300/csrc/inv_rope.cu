@@ -193,6 +193,8 @@ __device__ __forceinline__ void unit_loop(const RopeParams& p, const RopeIdx& ix
 
 template <bool QUANT, bool INTERLEAVED>
 __global__ void __launch_bounds__(kRopeThreads, 4) inv_rope_kernel(const RopeParams p, const RopeIdx ix) {
+  pdl_launch_dependents();  // programmatic dependent launch (see launch_pdl)
+  pdl_wait();
   bool bad = false;
   unit_loop<QUANT, INTERLEAVED, false>(p, ix, bad);
   unit_loop<QUANT, INTERLEAVED, true>(p, ix, bad);
@@ -210,8 +212,7 @@ cudaError_t launch_v(const RopeParams& p, const RopeIdx& ix, cudaStream_t stream
   const int64_t want = (int64_t)sm_count() * per_sm;
   const int64_t need = (units + 2 * kRopeThreads - 1) / (2 * kRopeThreads);  // 2 units a lane
   const int grid = (int)(need < want ? need : want);
-  kern<<<grid, kRopeThreads, 0, stream>>>(p, ix);
-  return cudaGetLastError();
+  return launch_pdl(kern, grid, kRopeThreads, 0, stream, p, ix);
 }
 
 }  // namespace

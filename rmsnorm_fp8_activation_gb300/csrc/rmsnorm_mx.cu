@@ -96,6 +96,8 @@ static __device__ __noinline__ float row_ms_exact(const uint4* row, int n, df S,
 template <int QS, int KS>
 __global__ void __launch_bounds__(kWarps * 32, (QS + KS >= 8) ? 2 : 3) rmsnorm_mx_kernel(const MxParams p) {
   constexpr bool RESIDENT = QS > 0;
+  pdl_launch_dependents();  // programmatic dependent launch (see launch_pdl)
+  pdl_wait();
   const int lane = threadIdx.x & 31;
   const int64_t gwarp = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5);
   const int64_t nwarps = (int64_t)gridDim.x * kWarps;
@@ -279,6 +281,8 @@ static_assert(kStagedHeader % 128 == 0, "row slots start 128-byte aligned");
 
 __global__ void __launch_bounds__(kStagedMaxWarps * 32) rmsnorm_mx_tma(const MxParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
+  pdl_launch_dependents();  // programmatic dependent launch (see launch_pdl)
+  pdl_wait();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, wpb = blockDim.x >> 5;
   const int64_t gwarp = (int64_t)blockIdx.x * wpb + warp;
   const int64_t nwarps = (int64_t)gridDim.x * wpb;
@@ -495,10 +499,16 @@ __global__ void __launch_bounds__(kRowsMaxWarps * 32, 1) rmsnorm_mx_rows(const M
     bulk_g2s(dst, p.q + m * p.q_stride, qbytes, bar);
     if (kbytes) bulk_g2s(dst + qbytes, p.kv + m * p.kv_stride, kbytes, bar);
   };
+  // programmatic dependent launch (see launch_pdl): shared-memory set-up may
+  // overlap the previous kernel; global memory only after pdl_wait
+  pdl_launch_dependents();
   if (lane == 0) {
     for (int s = 0; s < nslot; ++s) mbar_init(smem_u32(&bars[s]), 1);
     if (warp == 0) mbar_init(smem_u32(wbar), 1);
     asm volatile("fence.mbarrier_init.release.cluster;\n fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  pdl_wait();
+  if (lane == 0) {
     for (int s = 0; s < nslot; ++s) {
       const int64_t m = gwarp + s * nwarps;
       if (m < p.M) issue(s, m);
@@ -655,8 +665,7 @@ cudaError_t launch_rows_v(const MxParams& p, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   const int64_t need = (p.M + w - 1) / w;
   const int grid = (int)(need < sms ? need : sms);
-  kern<<<grid, w * 32, smem, stream>>>(p, nslot);
-  return cudaGetLastError();
+  return launch_pdl(kern, grid, w * 32, smem, stream, p, nslot);
 }
 
 template <int QR>
@@ -694,8 +703,7 @@ cudaError_t launch_staged(const MxParams& p, cudaStream_t stream) {
   const int64_t want = (int64_t)sm_count() * per_sm;
   const int64_t need = (p.M + best_w - 1) / best_w;
   const int grid = (int)(need < want ? need : want);
-  rmsnorm_mx_tma<<<grid, best_w * 32, smem, stream>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(rmsnorm_mx_tma, grid, best_w * 32, smem, stream, p);
 }
 
 template <int QS, int KS>
@@ -708,8 +716,7 @@ cudaError_t launch_variant(const MxParams& p, cudaStream_t stream) {
   const int64_t want = (int64_t)sm_count() * per_sm;
   const int64_t need = (p.M + kWarps - 1) / kWarps;
   const int grid = (int)(need < want ? need : want);
-  kern<<<grid, kWarps * 32, 0, stream>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(kern, grid, kWarps * 32, 0, stream, p);
 }
 
 }  // namespace

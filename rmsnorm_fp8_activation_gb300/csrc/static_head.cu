@@ -98,6 +98,8 @@ __device__ __forceinline__ uint32_t quot_pair(uint32_t x, const HeadConst& hc) {
 template <bool DYN>
 __global__ void __launch_bounds__(kThreads) static_head_kernel(const Flat f) {
   __shared__ HeadConst hcs[3 * kMaxHeads];
+  pdl_launch_dependents();  // programmatic dependent launch (see launch_pdl)
+  pdl_wait();
   const int nh = 3 * f.H;
   bool any_bad = false;
   for (int i = threadIdx.x; i < nh; i += blockDim.x) {
@@ -176,8 +178,10 @@ __global__ void __launch_bounds__(kThreads) static_head_kernel(const Flat f) {
 template <bool UNIFORM>
 __global__ void __launch_bounds__(kThreads) head_amax_kernel(const Flat f) {
   __shared__ int hmax[3 * kMaxHeads];
+  pdl_launch_dependents();  // programmatic dependent launch (see launch_pdl)
   const int nh = f.ntensors * f.H;
   for (int i = threadIdx.x; i < nh; i += blockDim.x) hmax[i] = 0;
+  pdl_wait();
   __syncthreads();
   const uint32_t stride = gridDim.x * blockDim.x;
   const uint32_t first = blockIdx.x * blockDim.x + threadIdx.x;
@@ -290,11 +294,9 @@ cudaError_t launch_amax_pass(const Flat& f, uint32_t max_chunks, cudaStream_t st
   if (e != cudaSuccess) return e;
   if (unit <= (uint64_t)want) {
     const int g = (int)((uint64_t)want / unit * unit);
-    head_amax_kernel<true><<<g, kThreads, 0, stream>>>(f);
-  } else {
-    head_amax_kernel<false><<<grid, kThreads, 0, stream>>>(f);
+    return launch_pdl(head_amax_kernel<true>, g, kThreads, 0, stream, f);
   }
-  return cudaGetLastError();
+  return launch_pdl(head_amax_kernel<false>, grid, kThreads, 0, stream, f);
 }
 
 }  // namespace
@@ -305,8 +307,7 @@ cudaError_t launch_static(const StaticParams& p, cudaStream_t stream) {
   int grid = 0;
   cudaError_t e = persistent_grid(static_head_kernel<false>, chunks, &grid);
   if (e != cudaSuccess) return e;
-  static_head_kernel<false><<<grid, kThreads, 0, stream>>>(f);
-  return cudaGetLastError();
+  return launch_pdl(static_head_kernel<false>, grid, kThreads, 0, stream, f);
 }
 
 // Dynamic per-head quantisation: zero the maxima, the amax pass, then the
@@ -325,8 +326,7 @@ cudaError_t launch_dynamic(const DynamicParams& p, cudaStream_t stream) {
   int grid = 0;
   e = persistent_grid(static_head_kernel<true>, chunks, &grid);
   if (e != cudaSuccess) return e;
-  static_head_kernel<true><<<grid, kThreads, 0, stream>>>(f);
-  return cudaGetLastError();
+  return launch_pdl(static_head_kernel<true>, grid, kThreads, 0, stream, f);
 }
 
 // Calibration: the running per-head maxima of one tensor, folded into amax.
