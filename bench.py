@@ -588,6 +588,31 @@ def ours(args, rank: int, world: int, local_rank: int) -> None:
     print(json.dumps(line), flush=True)
 
 
+def profile_case(args) -> None:
+    """One call repeated (for a profiler): the inverse-RoPE producer on the
+    o-projection workload, or the decode-sized gated call."""
+    import torch
+    import synth
+    import rmsnorm_fp8_activation_gb300 as B
+    from rmsnorm_fp8_activation_gb300 import build as _build
+    _build.build()
+    W = synth.workloads()
+    d16 = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).cuda().view(torch.bfloat16)
+    if args.case == "inv_rope":
+        w = W["inv_rope_mx"]
+        o = d16(w.o()).view(w.T, w.H, w.D)
+        pos, cs = torch.from_numpy(w.positions()).cuda(), torch.from_numpy(w.cos_sin()).cuda()
+        fn = lambda: B.fp8n_inv_rope_quant_mx(o, pos, cs, w.rope_off, w.rope_dim)
+    else:
+        w = W["gated_small"]
+        x, g, wt = d16(w.x()), d16(w.gate()), d16(w.weight())
+        fn = lambda: B.fp8n_gated_rmsnorm_quant_token(x, g, wt, w.eps, w.act)
+    for _ in range(args.warmup + args.steps):
+        fn()
+    torch.cuda.synchronize()
+    print(json.dumps({"case": args.case, "calls": args.warmup + args.steps}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -596,6 +621,9 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--small", action="store_true",
                     help="profiling case (see make_inputs); prints kernel times only")
+    ap.add_argument("--case", choices=["inv_rope", "decode"], default=None,
+                    help="profiling case: only the inverse-RoPE producer on its workload, or only "
+                         "the decode-sized gated call, --steps times back to back")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -606,7 +634,9 @@ def main():
         import torch.distributed as dist
         torch.cuda.set_device(local_rank)
         dist.init_process_group("nccl")
-    if args.impl == "reference":
+    if args.case is not None:
+        profile_case(args)
+    elif args.impl == "reference":
         reference_arm(args, rank, world)
     else:
         ours(args, rank, world, local_rank)
