@@ -289,6 +289,9 @@ def side_measurements(dev, d16, inp_c) -> dict:
         ts = []
         for _ in range(n):
             fsum.copy_(flush.view(torch.int64).sum())  # evicts L2 with clean lines
+            # keep the GPU busy while the host enqueues the call, so that no host
+            # time falls between the two events
+            torch.cuda._sleep(200000)
             e0 = torch.cuda.Event(enable_timing=True)
             e1 = torch.cuda.Event(enable_timing=True)
             e0.record()

@@ -415,14 +415,15 @@ __global__ void __launch_bounds__(kStagedMaxWarps * 32) rmsnorm_mx_tma(const MxP
 //
 // The fused q/kv producer for rows of at most kRowsMaxQRounds x 512 q and
 // kRowsMaxKRounds x 256 kv elements.  One CTA per SM; warp w of the grid walks
-// rows w, w + W, w + 2W, ... (W = warps in the grid) through `nslot`
-// shared-memory slots of its own, each filled by cp.async.bulk copies on its
-// own mbarrier; the slot is refilled with the row nslot steps ahead as soon as
-// the row is done.  Every warp requests its first rows before anything else,
-// and the weights arrive by one more bulk copy on a CTA-wide mbarrier, so no
-// warp waits at a block barrier for global memory.  Shared memory fits as many
-// warps as there are row pairs to hold, so at the q/kv workload's size every
-// row of an SM is in flight from the start.
+// rows w, w + W, w + 2W, ... (W = warps in the grid) through two shared-memory
+// slots of its own, each filled by cp.async.bulk copies on its own mbarrier:
+// a warp requests its first row before anything else and each next row as
+// soon as the current one has landed, so one row is in flight while one is
+// computed.  (Requesting every row of an SM at the start made each warp's
+// first row arrive anywhere in the whole read window, and the warps then
+// waited and computed in lock-step.)  The weights arrive by one more bulk copy
+// on a CTA-wide mbarrier, so no warp waits at a block barrier for global
+// memory.
 //
 // Lane layout.  q round j: lane l owns the sixteen elements of half-block
 // hb = 32j + l (chunks 2hb and 2hb + 1), so an MX block is the lane pair
@@ -509,10 +510,9 @@ __global__ void __launch_bounds__(kRowsMaxWarps * 32, 1) rmsnorm_mx_rows(const M
   }
   pdl_wait();
   if (lane == 0) {
-    for (int s = 0; s < nslot; ++s) {
-      const int64_t m = gwarp + s * nwarps;
-      if (m < p.M) issue(s, m);
-    }
+    // one row up front: the first rows of all warps (half the bytes of two each)
+    // land sooner, and every later row is requested as its predecessor lands
+    if (gwarp < p.M) issue(0, gwarp);
     if (warp == 0) {
       const uint32_t bar = smem_u32(wbar), dst = smem_u32(smem + kRowsHeader);
       mbar_expect_tx(bar, slot_bytes);
@@ -534,6 +534,12 @@ __global__ void __launch_bounds__(kRowsMaxWarps * 32, 1) rmsnorm_mx_rows(const M
     if (__any_sync(0xFFFFFFFFu, timeout)) {  // the whole warp stops (lane 0 drains)
       timeout = true;
       break;
+    }
+    // the next row goes into the other slot, which held the row before this one
+    // (done: every lane passed the __syncwarp that ended its iteration)
+    if (lane == 0 && m + nwarps < p.M) {
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      issue((it + 1) % nslot, m + nwarps);
     }
     const uint4* sq = reinterpret_cast<const uint4*>(slots + (size_t)s * slot_bytes);
     const uint4* sk = sq + qch;
@@ -622,22 +628,13 @@ __global__ void __launch_bounds__(kRowsMaxWarps * 32, 1) rmsnorm_mx_rows(const M
       const int c = 32 * j + lane;
       if (c < kch) *reinterpret_cast<uint4*>(ko + 8 * c) = norm_chunk4(sk[c], wk[c], rk);
     }
-    // the slot is free: request the row nslot steps ahead into it
-    __syncwarp();
-    if (lane == 0) {
-      const int64_t mn = m + (int64_t)nslot * nwarps;
-      if (mn < p.M) {
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        issue(s, mn);
-      }
-    }
+    __syncwarp();  // every lane is done with slot s before it is refilled
   }
   if (timeout && lane == 0) {
+    // the row whose wait gave up is the only one in flight
     if (p.status) atomicOr(p.status, kStatusTimeout);
-    for (int i = it; i < it + nslot; ++i) {
-      const int64_t mi = gwarp + (int64_t)i * nwarps;
-      if (mi < p.M) mbar_wait(smem_u32(&bars[i % nslot]), (uint32_t)(i / nslot) & 1u, kWaitLimit);
-    }
+    if (gwarp + (int64_t)it * nwarps < p.M)
+      mbar_wait(smem_u32(&bars[it % nslot]), (uint32_t)(it / nslot) & 1u, kWaitLimit);
   }
   // the weights' copy has landed before the CTA's shared memory goes away
   if (threadIdx.x == 0) mbar_wait(smem_u32(wbar), 0u, kWaitLimit);
