@@ -304,6 +304,7 @@ __global__ void __launch_bounds__(512) gated_token_tma(const GatedParams p, int 
   if (M::norm)
     for (int i = tid; i < p.D / 8; i += blockDim.x)
       reinterpret_cast<uint4*>(wsm)[i] = reinterpret_cast<const uint4*>(p.weight)[i];
+  for (int i = tid; i < 64; i += blockDim.x) red[i] = 0u;  // both halves of the warp maxima
   __syncthreads();
   if (LUT) {  // filled while the first rows are in flight
     lut_fill<ACT>(reinterpret_cast<uint32_t*>(lut), tid, blockDim.x);
@@ -391,12 +392,12 @@ __global__ void __launch_bounds__(512) gated_token_tma(const GatedParams p, int 
         for (int k = 0; k < 4; ++k) am2 = amax_step(am2, y[c][k]);
       }
     }
+    // the token amax as bf16 bits: non-negative bf16 values (NaN above
+    // infinity) order as unsigned integers, so one warp reduction takes it
     uint32_t* redb = red + (it & 1) * 32;
     if (M::quant) {
-      float amax = fmax_nan(bf16_lo(am2), bf16_hi(am2));
-#pragma unroll
-      for (int m = 16; m >= 1; m >>= 1) amax = fmax_nan(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, m));
-      if (lane == 0) redb[warp] = __float_as_uint(amax);
+      const uint32_t wmax = __reduce_max_sync(0xFFFFFFFFu, max(am2 & 0xFFFFu, am2 >> 16));
+      if (lane == 0) redb[warp] = wmax;
     }
     // every thread is done with stage s and has published its warp's amax; a
     // wait that gave up in any thread stops the whole CTA (thread 0 drains)
@@ -418,9 +419,13 @@ __global__ void __launch_bounds__(512) gated_token_tma(const GatedParams p, int 
       }
       continue;
     }
-    float tam = __uint_as_float(redb[0]);
-    for (int w = 1; w < nwarps; ++w) tam = fmax_nan(tam, __uint_as_float(redb[w]));
-    const float scale = scale_of(tam);
+    uint32_t tbits = 0u;  // the slots past the last warp hold 0
+    for (int w = 0; w < nwarps; w += 4) {
+      const uint4 v = *reinterpret_cast<const uint4*>(redb + w);
+      tbits = max(max(tbits, v.x), max(v.y, max(v.z, v.w)));
+    }
+    // (max.NaN makes a NaN amax the canonical NaN)
+    const float scale = scale_of(fmax_nan(__uint_as_float(tbits << 16), 0.0f));
     if (tid == 0) p.scale[t] = scale;
     if (active) {
       const TokenQuant tq(scale);

@@ -463,17 +463,15 @@ __device__ __forceinline__ df2 shfl_xor_df2(df2 v, int lane_mask) {
 // and one correction gives the nearest binary32 of S / n except within about
 // 2^-46 S of a rounding boundary, which the uncertainty test flags.  k: the
 // additions of each running sum behind S.
+// Both forms are evaluated and one is selected, so that lanes working on rows
+// of different lengths do not diverge.
 __device__ __forceinline__ float row_ms_k(df S, int n, float inv_n, bool n_pow2, int k,
                                           bool* unsure) {
   const float nf = (float)n;
-  float ms;
-  if (n_pow2) {
-    ms = __fmul_rn(__fadd_rn(S.h, S.l), inv_n);
-  } else {
-    const float q = __fmul_rn(S.h, inv_n);
-    const float rem = __fmaf_rn(-q, nf, S.h);
-    ms = __fadd_rn(q, __fmul_rn(__fadd_rn(rem, S.l), inv_n));
-  }
+  const float ms_pow2 = __fmul_rn(__fadd_rn(S.h, S.l), inv_n);
+  const float q = __fmul_rn(S.h, inv_n);
+  const float rem = __fmaf_rn(-q, nf, S.h);
+  const float ms = n_pow2 ? ms_pow2 : __fadd_rn(q, __fmul_rn(__fadd_rn(rem, S.l), inv_n));
   *unsure = ms_uncertain(S, nf, ms, __fmaf_rn(S.h, sumsq_rel_err(k, 6), nf * 0x1p-149f));
   return ms;
 }
@@ -573,15 +571,22 @@ __global__ void __launch_bounds__(kRowsMaxWarps * 32, 1) rmsnorm_mx_rows(const M
     df2 S = {f2(vq.h, vk.h), f2(vq.l, vk.l)};
 #pragma unroll
     for (int o = 16; o >= 1; o >>= 1) S = df2_add(S, shfl_xor_df2(S, o));
+    // the scalar tail once for both rows: q's mean square and factor in the
+    // even lanes, kv's in the odd lanes, then broadcast from lanes 0 and 1
     const float2 sh = unf2(S.h), sl = unf2(S.l);
     const df Sq = {sh.x, sl.x}, Sk = {sh.y, sl.y};
-    bool uq = false, uk = false;
-    float msq = row_ms_k(Sq, p.Nq, inv_nq, q_pow2, 8 * QR, &uq);
-    float msk = KR ? row_ms_k(Sk, p.Nkv, inv_nk, k_pow2, 4 * KR, &uk) : 0.0f;
-    if (uq) msq = row_ms_exact(sq, p.Nq, Sq, 2 * QR, msq, lane);  // rare; warp-uniform
-    if (KR && uk) msk = row_ms_exact(sk, p.Nkv, Sk, KR, msk, lane);
-    const f2_t rq = splat2(rms_factor(msq, p.eps));
-    const f2_t rk = splat2(KR ? rms_factor(msk, p.eps) : 0.0f);
+    const bool odd = KR && (lane & 1);
+    bool u = false;
+    const float ms = row_ms_k(odd ? Sk : Sq, odd ? p.Nkv : p.Nq, odd ? inv_nk : inv_nq,
+                              odd ? k_pow2 : q_pow2, odd ? 4 * KR : 8 * QR, &u);
+    const uint32_t unsure = __ballot_sync(0xFFFFFFFFu, u);
+    float msq = __shfl_sync(0xFFFFFFFFu, ms, 0);
+    float msk = KR ? __shfl_sync(0xFFFFFFFFu, ms, 1) : 0.0f;
+    if (unsure & 1u) msq = row_ms_exact(sq, p.Nq, Sq, 2 * QR, msq, lane);  // rare; warp-uniform
+    if (KR && (unsure & 2u)) msk = row_ms_exact(sk, p.Nkv, Sk, KR, msk, lane);
+    const float r = rms_factor(odd ? msk : msq, p.eps);
+    const f2_t rq = splat2(__shfl_sync(0xFFFFFFFFu, r, 0));
+    const f2_t rk = splat2(KR ? __shfl_sync(0xFFFFFFFFu, r, 1) : 0.0f);
 
     // pass 2: q -> MXFP8, kv -> bf16, read from the slot again
     uint8_t* qo = p.q_out + m * p.q_out_stride;

@@ -192,6 +192,10 @@ def test_mx_workload_prefix():
 @pytest.mark.parametrize("M,Nq,Nkv", [
     (1, 32, 0), (3, 32, 8), (5, 96, 40), (7, 1536, 512), (3, 2048, 2048), (2, 4096, 64),
     (2, 16384, 16384), (9, 224, 8), (33, 64, 24),
+    # the row kernel's q/kv register layouts: 2 and 4 q chunks of 512, 3 and 4 kv chunks of 256
+    (5, 1024, 256), (4, 2048, 1024), (6, 544, 768), (3, 1536, 0),
+    # more rows than warps on the grid, so that each warp's two slots are refilled
+    (9000, 544, 40), (4257, 32, 8),
 ])
 def test_mx_shapes(M, Nq, Nkv):
     q = synth.bf16_normal(7, 21 + Nq, M * Nq, sigma=1.4, outlier_p=0.01,
