@@ -21,8 +21,8 @@
 // it too, so it comes from L1), with interleaved pairs it is the chunk itself.
 // The rotation takes binary32 products and sums through the rounding
 // intrinsics (never contracted into a fused multiply-add).  An MX block is
-// two neighbouring lanes: max.xorsign.abs over the lane's eight bf16 pairs and
-// one xor-shuffle give its amax.
+// two neighbouring lanes: the largest magnitude over the lane's eight bf16
+// pairs and one xor-shuffle give its amax.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -168,11 +168,10 @@ __device__ __forceinline__ void unit_loop(const RopeParams& p, const RopeIdx& ix
       }
       const uint32_t* a = &v[j][0].x;
       const uint32_t* b = &v[j][1].x;
-      uint32_t am = max_abs2(max_abs2(max_abs2(a[0], a[1]), max_abs2(a[2], a[3])),
-                             max_abs2(max_abs2(b[0], b[1]), max_abs2(b[2], b[3])));
-      am = max_abs2(am, __shfl_xor_sync(0xFFFFFFFFu, am, 1));
+      uint32_t am = absmax8(a, b);
+      am = max_nan_bf16x2(am, __shfl_xor_sync(0xFFFFFFFFu, am, 1));
       if (!ok) continue;
-      const uint32_t mag = am & 0x7FFF7FFFu;
+      const uint32_t mag = am;
       const uint32_t code = mx_code(max(mag & 0xFFFFu, mag >> 16));
       if ((lane & 1) == 0) p.scale[(int64_t)tk[j] * p.scale_stride + (col >> 5)] = (uint8_t)code;
       uint4 o;

@@ -606,10 +606,9 @@ __global__ void __launch_bounds__(kRowsMaxWarps * 32, 1) rmsnorm_mx_rows(const M
       uint32_t y[8];
       norm_chunk(x0, w0, rq, y);
       norm_chunk(x1, w1, rq, y + 4);
-      uint32_t am = max_abs2(max_abs2(max_abs2(y[0], y[1]), max_abs2(y[2], y[3])),
-                             max_abs2(max_abs2(y[4], y[5]), max_abs2(y[6], y[7])));
-      am = max_abs2(am, __shfl_xor_sync(0xFFFFFFFFu, am, 1));
-      const uint32_t mag = am & 0x7FFF7FFFu;
+      uint32_t am = absmax8(y, y + 4);
+      am = max_nan_bf16x2(am, __shfl_xor_sync(0xFFFFFFFFu, am, 1));
+      const uint32_t mag = am;
       const uint32_t code = mx_code(max(mag & 0xFFFFu, mag >> 16));
       if (ok) {
         if ((lane & 1) == 0) so[hb >> 1] = (uint8_t)code;
