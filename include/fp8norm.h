@@ -383,6 +383,25 @@ fp8n_status fp8n_head_amax(const void* x, int64_t tok_stride, int64_t head_strid
 fp8n_status fp8n_gate_act_bf16(const void* g, int64_t n, fp8n_act act, void* out,
                                fp8n_stream_t stream);
 
+/* Target of fp8n_convert_f32. */
+typedef enum { FP8N_CVT_BF16 = 0, FP8N_CVT_E4M3 = 1 } fp8n_cvt;
+
+/*
+ * The two roundings of binary32 values that every operation above ends with,
+ * alone: out[i] = bf16(in[i]) (nearest-even, 2 bytes each; NaN stays NaN) or
+ * out[i] = e4m3(in[i]) (OCP E4M3 "fn": saturating nearest-even, |v| above 448
+ * and infinities to +-448, NaN to 0x7F/0xFF, signed zeros kept; 1 byte each),
+ * by the same device conversions the kernels use.  Sources: the torch
+ * reference helper in "[ROCm][Kimi-K3] Fuse gated RMSNorm with per-token FP8
+ * for KDA o_proj" (values rounded to the bf16 activation dtype; codes in the
+ * e4m3 format whose largest value 448 is the quantiser's fp8 maximum) and the
+ * OCP 8-bit floating point specification (OFP8) for E4M3.
+ * in: fp32 [n], 4-byte aligned device pointer; out: [n] bf16 (2-byte aligned)
+ * or uint8; n >= 0; FP8N_ERR_UNSUPPORTED for another target.
+ */
+fp8n_status fp8n_convert_f32(const float* in, int64_t n, fp8n_cvt to, void* out,
+                             fp8n_stream_t stream);
+
 /*
  * Synchronous helper: reads n fp32 descales from device memory (through a
  * host copy on `stream`, which it synchronises) and returns

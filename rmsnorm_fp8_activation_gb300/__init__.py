@@ -67,6 +67,8 @@ def lib() -> ctypes.CDLL:
         L.fp8n_static_head_quant.restype = ctypes.c_int
         L.fp8n_gate_act_bf16.argtypes = [P, i64, ctypes.c_int, P, P]
         L.fp8n_gate_act_bf16.restype = ctypes.c_int
+        L.fp8n_convert_f32.argtypes = [P, i64, ctypes.c_int, P, P]
+        L.fp8n_convert_f32.restype = ctypes.c_int
         L.fp8n_check_descales.argtypes = [P, i32, P]
         L.fp8n_check_descales.restype = ctypes.c_int
         L.fp8n_gated_rmsnorm_bf16.argtypes = [
@@ -262,6 +264,23 @@ def fp8n_gate_act_bf16(g, act: int = ACT_SIGMOID, out=None, stream=None):
         out = torch.empty(g.shape, dtype=torch.bfloat16, device=g.device)
     _check("fp8n_gate_act_bf16", lib().fp8n_gate_act_bf16(
         _ptr(g), g.numel(), act, _ptr(out), _stream(stream)))
+    return out
+
+
+CVT_BF16 = 0
+CVT_E4M3 = 1
+
+
+def fp8n_convert_f32(x, to: int, out=None, stream=None):
+    """bf16 (to=CVT_BF16) or E4M3 codes (to=CVT_E4M3, uint8) of each value of a
+    contiguous fp32 CUDA tensor, by the kernels' own conversions."""
+    if not x.is_cuda or x.dtype != torch.float32 or not x.is_contiguous():
+        raise ValueError("x must be a contiguous float32 CUDA tensor")
+    if out is None:
+        out = torch.empty(x.shape, dtype=torch.bfloat16 if to == CVT_BF16 else torch.uint8,
+                          device=x.device)
+    _check("fp8n_convert_f32", lib().fp8n_convert_f32(_ptr(x), x.numel(), to, _ptr(out),
+                                                      _stream(stream)))
     return out
 
 

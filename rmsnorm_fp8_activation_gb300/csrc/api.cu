@@ -537,6 +537,17 @@ fp8n_status fp8n_gate_act_bf16(const void* g, int64_t n, fp8n_act act, void* out
                                            (cudaStream_t)stream));
 }
 
+fp8n_status fp8n_convert_f32(const float* in, int64_t n, fp8n_cvt to, void* out,
+                             fp8n_stream_t stream) {
+  if (n < 0) return FP8N_ERR_SHAPE;
+  if (to != FP8N_CVT_BF16 && to != FP8N_CVT_E4M3) return FP8N_ERR_UNSUPPORTED;
+  if (n == 0) return FP8N_OK;
+  if (!in || !out) return FP8N_ERR_NULL;
+  if (((uintptr_t)in & 3u) || (to == FP8N_CVT_BF16 && ((uintptr_t)out & 1u)))
+    return FP8N_ERR_MISALIGNED;
+  return cuda_status(fp8n::launch_convert(in, n, (int)to, out, (cudaStream_t)stream));
+}
+
 fp8n_status fp8n_check_descales(const float* descale, int32_t n, fp8n_stream_t stream) {
   if (n < 1 || n > 65536) return FP8N_ERR_SHAPE;
   if (!descale) return FP8N_ERR_NULL;

@@ -122,6 +122,7 @@ cudaError_t launch_static(const StaticParams& p, cudaStream_t stream);
 cudaError_t launch_dynamic(const DynamicParams& p, cudaStream_t stream);
 cudaError_t launch_head_amax(const AmaxParams& p, cudaStream_t stream);
 cudaError_t launch_inv_rope(const RopeParams& p, cudaStream_t stream);
+cudaError_t launch_convert(const float* in, int64_t n, int to, void* out, cudaStream_t stream);
 cudaError_t launch_gate_act(const uint16_t* g, int64_t n, int act, uint16_t* out,
                             cudaStream_t stream);
 

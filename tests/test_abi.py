@@ -126,6 +126,16 @@ def test_gate_act_and_check_validation(L):
     assert L.fp8n_check_descales(None, 4, None) == NULL
 
 
+def test_convert_validation(L):
+    assert L.fp8n_convert_f32(P16, 0, 0, P16, None) == OK
+    assert L.fp8n_convert_f32(P16, -1, 0, P16, None) == SHAPE
+    assert L.fp8n_convert_f32(P16, 4, 2, P16, None) == UNSUPPORTED
+    assert L.fp8n_convert_f32(None, 4, 1, P16, None) == NULL
+    assert L.fp8n_convert_f32(P16, 4, 1, None, None) == NULL
+    assert L.fp8n_convert_f32(P16 + 2, 4, 1, P16, None) == MISALIGNED
+    assert L.fp8n_convert_f32(P16, 4, 0, P16 + 1, None) == MISALIGNED
+
+
 def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
     import rmsnorm_fp8_activation_gb300 as B
     monkeypatch.setattr(B, "_lib", None)
