@@ -102,6 +102,51 @@ def test_quant_token_special_rows(N):
     assert np.array_equal(got, want)
 
 
+def _rows_for_amax(A: int, N: int) -> np.ndarray:
+    """Rows of N bf16 values that begin with the positive bf16 A and together
+    hold every bf16 value of magnitude at most A, both signs (zeros pad the
+    last row): each row's amax, and so its scale RN32(A / 448), is fixed."""
+    mags = np.arange(A + 1, dtype=np.uint32)
+    vals = np.concatenate([mags, mags | 0x8000]).astype(np.uint16)
+    per = N - 1
+    nrow = -(-vals.size // per)
+    body = np.zeros(nrow * per, np.uint16)
+    body[:vals.size] = vals
+    return np.concatenate([np.full((nrow, 1), A, np.uint16), body.reshape(nrow, per)], axis=1)
+
+
+def test_quant_token_every_numerator_under_many_scales():
+    """The per-token quotient e4m3(RN32(y / scale)) for every bf16 numerator
+    up to the row's amax, under about 2,000 scales: amax = 448 * 2^k (exact
+    power-of-two scales, so y / scale hits E4M3 ties exactly), amax with a
+    short mantissa (scales with few bits), subnormal amax, and random amax
+    across the exponent range; codes and scales bit for bit."""
+    rng = np.random.default_rng(41)
+    amax = [0x43E0 + (k << 7) for k in range(-134, 120)]               # 448 * 2^k
+    for m in (0x00, 0x40, 0x20, 0x60, 0x10, 0x30, 0x50, 0x70, 0x08, 0x7F):
+        amax += [((e << 7) | m) for e in range(1, 255, 3)]              # short mantissas
+    amax += [0x0001, 0x0002, 0x0040, 0x007F]                          # subnormal amax
+    amax += [int(a) for a in (rng.integers(1, 255, 1100) << 7) | rng.integers(0, 128, 1100)]
+    amax = sorted(set(amax))
+    N = 16384
+    y = np.concatenate([_rows_for_amax(A, N) for A in amax])
+    oc, os_ = B.fp8n_quant_token(dev16(y))
+    torch.cuda.synchronize()
+    got_c, got_s = oc.cpu().numpy(), os_.cpu().numpy()
+    want_c = np.empty_like(got_c)
+    want_s = np.empty_like(got_s)
+
+    def ref(a, b):
+        want_c[a:b], want_s[a:b] = O.quant_token(y[a:b])
+
+    O.sliced(ref, y.shape[0], min_slice=64)
+    print("division", {"scales": len(amax), "rows": int(y.shape[0]), "elements": int(y.size)})
+    assert np.array_equal(got_s.view(np.uint32), want_s.view(np.uint32))
+    bad = np.nonzero(got_c != want_c)
+    assert bad[0].size == 0, [(hex(int(y[t, j])), hex(int(got_c[t, j])), hex(int(want_c[t, j])))
+                              for t, j in zip(*bad)][:8]
+
+
 def test_quant_token_strided_rows():
     T, N = 70, 1024
     y = rows(5, T, N)
@@ -198,6 +243,36 @@ def test_quant_mx(M, N):
     wc, ws = O.quant_mx(y)
     assert np.array_equal(osc.cpu().numpy(), ws)         # E8M0: bit-exact
     assert np.array_equal(oc.cpu().numpy(), wc)          # exact power-of-two scaling
+
+
+def test_quant_mx_every_block_amax():
+    """One MX block for every non-negative bf16 pattern A (0 .. 0x7FFF:
+    zero, subnormals, normals, infinity, NaNs): the block holds A, -A and
+    thirty magnitudes spread below A, so its amax is A and its E8M0 code is
+    floor(log2 A) - 8 + 127 (clamped; 0xFF for infinity and NaN).  Scales
+    and element codes bit for bit against the oracle."""
+    A = np.arange(0x8000, dtype=np.uint32)
+    k = np.arange(30, dtype=np.uint32)
+    blocks = np.empty((0x8000, 32), np.uint32)
+    blocks[:, 0] = A
+    blocks[:, 1] = A | 0x8000
+    blocks[:, 2:] = (A[:, None] * k[None, :]) >> 5
+    blocks[:, 3::2] |= 0x8000                            # every other one negative
+    y = blocks.astype(np.uint16).reshape(64, 16384)
+    oc, osc = B.fp8n_quant_mx(dev16(y))
+    torch.cuda.synchronize()
+    wc, ws = O.quant_mx(y)
+    got_s = osc.cpu().numpy()
+    assert np.array_equal(got_s, ws)
+    e = (A >> 7).astype(np.int64)
+    lg = np.where(e > 0, e - 127, -133 + np.floor(np.log2(np.maximum(A & 0x7F, 1))).astype(np.int64))
+    code = np.clip(lg - 8, -127, 127) + 127
+    code = np.where(A == 0, 0, np.where(e == 0xFF, 0xFF, code))
+    assert np.array_equal(got_s.reshape(-1), code.astype(np.uint8))
+    got_c = oc.cpu().numpy()
+    bad = np.nonzero(got_c != wc)
+    assert bad[0].size == 0, [(hex(int(y[t, j])), hex(int(got_c[t, j])), hex(int(wc[t, j])))
+                              for t, j in zip(*bad)][:8]
 
 
 @pytest.mark.parametrize("M", [777, 8192])
