@@ -270,7 +270,8 @@ def side_measurements(dev, d16, inp_c) -> dict:
     """Median device time over 30 launches (L2 flushed before each) of: (A) at
     the gated_silu size fused and as gated norm -> bf16 -> per-token quant;
     (B) at the qkv_mx size fused and as RMSNorm -> bf16 -> MX quant plus the
-    kv RMSNorm; the dynamic per-head quantisation of the static_head
+    kv RMSNorm; the decode-sized (A) fused and as its two steps, replayed from
+    CUDA graphs; the dynamic per-head quantisation of the static_head
     workload (max pass + quantise pass); the inverse-RoPE + MXFP8 producer of
     the o-projection input, fused and as its two steps."""
     import torch
@@ -322,42 +323,45 @@ def side_measurements(dev, d16, inp_c) -> dict:
     xd, gd, wtd = d16(wd.x()), d16(wd.gate()), d16(wd.weight())
     od = torch.empty((wd.T, wd.H * wd.D), dtype=torch.uint8, device=dev)
     sd = torch.empty((wd.T,), dtype=torch.float32, device=dev)
+    yd = torch.empty((wd.T, wd.H * wd.D), dtype=torch.bfloat16, device=dev)
     cs = torch.cuda.Stream(device=dev)
-    with torch.cuda.stream(cs):
-        for _ in range(3):
-            B.fp8n_gated_rmsnorm_quant_token(xd, gd, wtd, wd.eps, wd.act, out=od, scale=sd)
-    cs.synchronize()
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph, stream=cs):
+
+    def fused_call():
         B.fp8n_gated_rmsnorm_quant_token(xd, gd, wtd, wd.eps, wd.act, out=od, scale=sd)
-    reps = 200
-    for _ in range(10):
-        graph.replay()
-    torch.cuda.synchronize()
-    g0 = torch.cuda.Event(enable_timing=True)
-    g1 = torch.cuda.Event(enable_timing=True)
-    g0.record()
-    for _ in range(reps):
-        graph.replay()
-    g1.record()
-    torch.cuda.synchronize()
-    small_us = 1e3 * g0.elapsed_time(g1) / reps
+
+    def unfused_call():  # the same result through the two steps
+        B.fp8n_gated_rmsnorm_bf16(xd, gd, wtd, wd.eps, wd.act, y=yd)
+        B.fp8n_quant_token(yd, out=od, scale=sd)
+
+    def graph_us(fn, per_graph: int, replays: int) -> float:
+        """Device time per fn() captured per_graph times in one CUDA graph."""
+        with torch.cuda.stream(cs):
+            for _ in range(3):
+                fn()
+        cs.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=cs):
+            for _ in range(per_graph):
+                fn()
+        for _ in range(5):
+            g.replay()
+        torch.cuda.synchronize()
+        g0 = torch.cuda.Event(enable_timing=True)
+        g1 = torch.cuda.Event(enable_timing=True)
+        g0.record()
+        for _ in range(replays):
+            g.replay()
+        g1.record()
+        torch.cuda.synchronize()
+        return 1e3 * g0.elapsed_time(g1) / (replays * per_graph)
+
+    small_us = graph_us(fused_call, 1, 200)
     # the same call as one node among 20 in a graph (as in a decode step's
     # graph): the graph's own launch is spread over its nodes
     nodes = 20
-    graph20 = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph20, stream=cs):
-        for _ in range(nodes):
-            B.fp8n_gated_rmsnorm_quant_token(xd, gd, wtd, wd.eps, wd.act, out=od, scale=sd)
-    for _ in range(5):
-        graph20.replay()
-    torch.cuda.synchronize()
-    g0.record()
-    for _ in range(20):
-        graph20.replay()
-    g1.record()
-    torch.cuda.synchronize()
-    small_node_us = 1e3 * g0.elapsed_time(g1) / (20 * nodes)
+    small_node_us = graph_us(fused_call, nodes, 20)
+    small_unfused_us = graph_us(unfused_call, 1, 200)
+    small_unfused_node_us = graph_us(unfused_call, nodes, 20)
     # a plain device copy of as many bytes as the q/kv producer moves (27.5 MB
     # read, 27.5 MB written): what one stream of this size takes here
     cp_src = torch.empty(wm.algorithmic_bytes() // 4, dtype=torch.int16, device=dev)
@@ -373,6 +377,11 @@ def side_measurements(dev, d16, inp_c) -> dict:
         "gated_small_graph_note": "56 x 12 x 128 sigmoid, one call per graph replay, inputs resident",
         "gated_small_graph_node_us": small_node_us,
         "gated_small_graph_node_note": "the same call as one of 20 nodes of a graph (per node)",
+        "gated_small_unfused_graph_us": small_unfused_us,
+        "gated_small_unfused_graph_node_us": small_unfused_node_us,
+        "gated_small_unfused_note": "the same result as fp8n_gated_rmsnorm_bf16 -> "
+                                    "fp8n_quant_token: per replay of the two calls, and per "
+                                    "pair as 20 pairs of nodes of one graph",
         "copy_55MB_us": copy_us,
         "copy_55MB_note": "torch device copy of the q/kv producer's algorithmic bytes (half read, "
                           "half written): a plain stream of this size, for context",
