@@ -476,7 +476,9 @@ __device__ __forceinline__ float row_ms_k(df S, int n, float inv_n, bool n_pow2,
   return ms;
 }
 
-template <int QR, int KR>
+// FULL: the rows fill every round (Nq = 512 QR, Nkv = 256 KR), so no lane
+// needs a bounds test.
+template <int QR, int KR, bool FULL>
 __global__ void __launch_bounds__(kRowsMaxWarps * 32, 1) rmsnorm_mx_rows(const MxParams p, int nslot) {
   extern __shared__ __align__(128) uint8_t smem[];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, wpb = blockDim.x >> 5;
@@ -548,11 +550,11 @@ __global__ void __launch_bounds__(kRowsMaxWarps * 32, 1) rmsnorm_mx_rows(const M
     for (int j = 0; j < QR; ++j) {
       const int hb = 32 * j + lane;
       uint4 a = make_uint4(0, 0, 0, 0), b = a, c = a;
-      if (hb < nhb) {
+      if (FULL || hb < nhb) {
         a = sq[2 * hb + rot];
         b = sq[2 * hb + 1 - rot];
       }
-      if (KR && j < KR && 32 * j + lane < kch) c = sk[32 * j + lane];
+      if (KR && j < KR && (FULL || 32 * j + lane < kch)) c = sk[32 * j + lane];
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         aq.add_sq((&a.x)[k]);
@@ -563,7 +565,7 @@ __global__ void __launch_bounds__(kRowsMaxWarps * 32, 1) rmsnorm_mx_rows(const M
 #pragma unroll
     for (int j = QR; j < KR; ++j) {
       uint4 c = make_uint4(0, 0, 0, 0);
-      if (32 * j + lane < kch) c = sk[32 * j + lane];
+      if (FULL || 32 * j + lane < kch) c = sk[32 * j + lane];
 #pragma unroll
       for (int k = 0; k < 4; ++k) ak.add_sq((&c.x)[k]);
     }
@@ -593,9 +595,9 @@ __global__ void __launch_bounds__(kRowsMaxWarps * 32, 1) rmsnorm_mx_rows(const M
     uint8_t* so = p.q_scale + m * p.q_scale_stride;
 #pragma unroll
     for (int j = 0; j < QR; ++j) {
-      if (32 * j >= nhb) break;  // warp-uniform
+      if (!FULL && 32 * j >= nhb) break;  // warp-uniform
       const int hb = 32 * j + lane;
-      const bool ok = hb < nhb;
+      const bool ok = FULL || hb < nhb;
       uint4 x0 = make_uint4(0, 0, 0, 0), x1 = x0, w0 = x0, w1 = x0;
       if (ok) {
         x0 = sq[2 * hb + rot];
@@ -611,7 +613,7 @@ __global__ void __launch_bounds__(kRowsMaxWarps * 32, 1) rmsnorm_mx_rows(const M
       const uint32_t mag = am;
       const uint32_t code = mx_code(max(mag & 0xFFFFu, mag >> 16));
       if (ok) {
-        if ((lane & 1) == 0) so[hb >> 1] = (uint8_t)code;
+        so[hb >> 1] = (uint8_t)code;  // both lanes of the block store the same byte
         uint32_t o[4];
         if (code == 0xFFu) {
           o[0] = o[1] = o[2] = o[3] = 0x7F7F7F7Fu;
@@ -630,7 +632,7 @@ __global__ void __launch_bounds__(kRowsMaxWarps * 32, 1) rmsnorm_mx_rows(const M
 #pragma unroll
     for (int j = 0; j < KR; ++j) {
       const int c = 32 * j + lane;
-      if (c < kch) *reinterpret_cast<uint4*>(ko + 8 * c) = norm_chunk4(sk[c], wk[c], rk);
+      if (FULL || c < kch) *reinterpret_cast<uint4*>(ko + 8 * c) = norm_chunk4(sk[c], wk[c], rk);
     }
     __syncwarp();  // every lane is done with slot s before it is refilled
   }
@@ -650,9 +652,9 @@ __global__ void __launch_bounds__(kRowsMaxWarps * 32, 1) rmsnorm_mx_rows(const M
 #ifndef FP8N_ROWS_WARPS
 #define FP8N_ROWS_WARPS kRowsMaxWarps
 #endif
-template <int QR, int KR>
+template <int QR, int KR, bool FULL>
 cudaError_t launch_rows_v(const MxParams& p, cudaStream_t stream) {
-  auto kern = rmsnorm_mx_rows<QR, KR>;
+  auto kern = rmsnorm_mx_rows<QR, KR, FULL>;
   const size_t slot = 2 * (size_t)(p.Nq + p.Nkv);
   const size_t budget = 227 * 1024 - 1024 - kRowsHeader - slot;  // less the weights
   const int nslot = kRowsMaxSlots;
@@ -669,13 +671,19 @@ cudaError_t launch_rows_v(const MxParams& p, cudaStream_t stream) {
   return launch_pdl(kern, grid, w * 32, smem, stream, p, nslot);
 }
 
+template <int QR, int KR>
+cudaError_t launch_rows_f(const MxParams& p, cudaStream_t stream) {
+  if (p.Nq == 512 * QR && p.Nkv == 256 * KR) return launch_rows_v<QR, KR, true>(p, stream);
+  return launch_rows_v<QR, KR, false>(p, stream);
+}
+
 template <int QR>
 cudaError_t launch_rows_q(const MxParams& p, int kr, cudaStream_t stream) {
   switch (kr) {
-    case 0: return launch_rows_v<QR, 0>(p, stream);
-    case 1: return launch_rows_v<QR, 1>(p, stream);
-    case 2: return launch_rows_v<QR, 2>(p, stream);
-    default: return launch_rows_v<QR, 4>(p, stream);
+    case 0: return launch_rows_f<QR, 0>(p, stream);
+    case 1: return launch_rows_f<QR, 1>(p, stream);
+    case 2: return launch_rows_f<QR, 2>(p, stream);
+    default: return launch_rows_f<QR, 4>(p, stream);
   }
 }
 
