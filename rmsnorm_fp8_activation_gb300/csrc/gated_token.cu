@@ -312,7 +312,10 @@ __global__ void __launch_bounds__(512) gated_token_tma(const GatedParams p, int 
   }
 
   const int seg = tid * 8 * CPT;  // first element of the thread's segment
-  const uint16_t* wseg = wsm + (seg % p.D);
+  // an idle thread (past the row) reads segment 0 and is masked out of the
+  // token maximum and the stores, so that no read needs a test
+  const int rseg = active ? seg : 0;
+  const uint16_t* wseg = wsm + (rseg % p.D);
   const float inv_d = 1.0f / (float)p.D;  // exact: D is a power of two here
   // error bound of a head's sum relative to S, plus the squares below 2^-126
   // that binary32 rounds (at most 2^-150 each)
@@ -324,7 +327,7 @@ __global__ void __launch_bounds__(512) gated_token_tma(const GatedParams p, int 
   for (int64_t t = blockIdx.x; t < p.T; t += gridDim.x, ++it) {
     const int s = it % nstage;
     if (!mbar_wait(smem_u32(&bars[s]), (uint32_t)(it / nstage) & 1u, kWaitLimitMain)) timeout = true;
-    const uint8_t* sx = stages + (size_t)s * stage_bytes + (size_t)seg * 2;
+    const uint8_t* sx = stages + (size_t)s * stage_bytes + (size_t)rseg * 2;
     const uint8_t* sg = sx + row_bytes;
 
     // pass 1: the head's sum of squares (x is read again in pass 2) and ms =
@@ -337,10 +340,10 @@ __global__ void __launch_bounds__(512) gated_token_tma(const GatedParams p, int 
     // path.  The lanes of a head agree on S, so a head is flagged as a whole.
     float ms = 0.0f;
     if (M::norm && M::quant) {
-      const df S = head_sum_fast<CPT, TPH>(sx, tid, active);
+      const df S = head_sum_fast<CPT, TPH>(sx, tid, true);
       ms = __fmul_rn(__fadd_rn(S.h, S.l), inv_d);
     } else if (M::norm) {
-      df S = head_sum<CPT, TPH>(sx, tid, active);
+      df S = head_sum<CPT, TPH>(sx, tid, true);
       const float err = __fmaf_rn(S.h, rel_err, sq_floor);
       bool unsure = S.h != 0.0f &&
                     __fadd_rn(S.h, __fadd_rn(S.l, err)) != __fadd_rn(S.h, __fsub_rn(S.l, err));
@@ -360,11 +363,8 @@ __global__ void __launch_bounds__(512) gated_token_tma(const GatedParams p, int 
 #pragma unroll
     for (int c = 0; c < CPT; ++c) {
       const int off = 16 * slot_of<CPT>(c, tid);
-      uint4 xv = make_uint4(0, 0, 0, 0), gv = xv;
-      if (active) {
-        xv = *reinterpret_cast<const uint4*>(sx + off);
-        if (M::gate) gv = *reinterpret_cast<const uint4*>(sg + off);
-      }
+      const uint4 xv = *reinterpret_cast<const uint4*>(sx + off);
+      const uint4 gv = M::gate ? *reinterpret_cast<const uint4*>(sg + off) : make_uint4(0, 0, 0, 0);
       const uint32_t *xw = &xv.x, *gw = &gv.x;
       uint32_t ga[4];
       if (M::gate) {
@@ -387,17 +387,18 @@ __global__ void __launch_bounds__(512) gated_token_tma(const GatedParams p, int 
 #pragma unroll
         for (int k = 0; k < 4; ++k) y[c][k] = xw[k];
       }
-      if (M::quant && active) {  // (an idle lane's y is not part of the row)
+      if (M::quant) {
 #pragma unroll
         for (int k = 0; k < 4; ++k) am2 = amax_step(am2, y[c][k]);
       }
     }
+    if (!active) am2 = 0u;  // an idle lane's y is not part of the row
     // the token amax as bf16 bits: non-negative bf16 values (NaN above
     // infinity) order as unsigned integers, so one warp reduction takes it
     uint32_t* redb = red + (it & 1) * 32;
     if (M::quant) {
       const uint32_t wmax = __reduce_max_sync(0xFFFFFFFFu, max(am2 & 0xFFFFu, am2 >> 16));
-      if (lane == 0) redb[warp] = wmax;
+      redb[warp] = wmax;  // (every lane stores the same value)
     }
     // every thread is done with stage s and has published its warp's amax; a
     // wait that gave up in any thread stops the whole CTA (thread 0 drains)

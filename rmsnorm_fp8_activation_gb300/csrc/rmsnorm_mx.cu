@@ -428,7 +428,7 @@ __global__ void __launch_bounds__(kStagedMaxWarps * 32) rmsnorm_mx_tma(const MxP
 // Lane layout.  q round j: lane l owns the sixteen elements of half-block
 // hb = 32j + l (chunks 2hb and 2hb + 1), so an MX block is the lane pair
 // (l, l ^ 1): its amax is the lane's running |max| over eight bf16 pairs and
-// one xor-shuffle, and the even lane stores the E8M0 code.  The two chunks are
+// one xor-shuffle, and both lanes store the E8M0 code.  The two chunks are
 // read in a rotated order (lanes with bit 2 set take the odd one first) so
 // that the eight 16-byte reads of a quarter-warp hit distinct bank groups.
 // kv round j: lane l owns chunk 32j + l.  The sums of squares of q and kv are
