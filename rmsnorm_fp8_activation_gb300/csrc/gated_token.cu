@@ -47,24 +47,6 @@ __device__ __forceinline__ float scale_of(float amax) {
   return div_rn(amax, 448.0f, 1.0f / 448.0f);
 }
 
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
-               : "memory");
-}
-
-__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
-                                         uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-          dst),
-      "l"(src), "r"(bytes), "r"(bar)
-      : "memory");
-}
-
 __device__ __forceinline__ float fmax_nan(float a, float b) {
   float d;
   asm("max.NaN.f32 %0, %1, %2;" : "=f"(d) : "f"(a), "f"(b));
@@ -408,7 +390,11 @@ __global__ void __launch_bounds__(512) gated_token_tma(const GatedParams p, int 
     }
     if (tid == 0) {
       const int64_t tn = t + (int64_t)nstage * gridDim.x;
-      if (tn < p.T) issue(s, tn);
+      if (tn < p.T) {
+        // the threads' reads of stage s come before the copy that overwrites it
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        issue(s, tn);
+      }
     }
     if (!M::quant) {
       if (active) {

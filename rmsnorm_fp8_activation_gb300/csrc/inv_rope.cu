@@ -12,17 +12,18 @@
 // producer: E8M0 code floor(log2 amax) - 8 + 127 per 32 elements, element
 // codes e4m3(y * 2^-e).
 //
-// GB300 design: an HBM stream.  Warps walk spans of 128 consecutive pairs of
-// 16-byte chunks of the flattened rows (lane l: pairs l, l+32, l+64, l+96,
-// read-only loads, eight chunks in flight), token and head indices by
-// multiply-shift division once per span.  The RoPE span starts on a chunk and holds whole chunk pairs, so a
-// chunk is rotated or passed through as a whole; with rotate-half pairs a
-// chunk's partner lies R/2 elements away in the same head (another lane reads
-// it too, so it comes from L1), with interleaved pairs it is the chunk itself.
-// The rotation takes binary32 products and sums through the rounding
-// intrinsics (never contracted into a fused multiply-add).  An MX block is
-// two neighbouring lanes: the largest magnitude over the lane's eight bf16
-// pairs and one xor-shuffle give its amax.
+// GB300 design: an HBM stream.  Work units are half MX blocks (two adjacent
+// 16-byte chunks of one head); a warp takes 64 units at a time (lane l: units
+// l and l + 32, read-only loads), the blocks of a head that meet the RoPE span
+// and the others in two separate loops, so that the rotation is warp-uniform
+// work.  The span starts on a chunk and holds whole chunks, so a chunk is
+// rotated or passed through as a whole; with rotate-half pairs a chunk's
+// partner lies R/2 elements away in the same head (another lane reads it too,
+// so it comes from L1), with interleaved pairs it is the chunk itself.  The
+// rotation takes binary32 products and sums through the rounding intrinsics
+// (never contracted into a fused multiply-add).  An MX block is two
+// neighbouring lanes: the largest magnitude over the lane's eight bf16 pairs
+// and one xor-shuffle give its amax.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -66,6 +67,35 @@ __device__ __forceinline__ uint32_t rot_pair(uint32_t x, uint32_t w, float c0, f
   return pack_bf16x2(rot1(bf16_lo(x), c0, bf16_lo(w), s0), rot1(bf16_hi(x), c1, bf16_hi(w), s1));
 }
 
+// Interleaved pairs (2k, 2k+1) of a chunk, with the angles cc, ss of its four
+// pairs: (x1, x2) -> (x1 c + x2 s, x2 c + (-x1) s).
+__device__ __forceinline__ void rot_interleaved(uint4& v, float4 cc, float4 ss) {
+  uint32_t* w = &v.x;
+  const float cv[4] = {cc.x, cc.y, cc.z, cc.w}, sv[4] = {ss.x, ss.y, ss.z, ss.w};
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const uint32_t swapped = __byte_perm(w[k], 0, 0x1032) ^ 0x80000000u;  // (x2, -x1)
+    w[k] = rot_pair(w[k], swapped, cv[k], cv[k], sv[k], sv[k]);
+  }
+}
+
+// Rotate-half pairs of a chunk with its partner chunk pv (already negated for
+// a chunk of the second half) and the angles of its eight pairs.
+__device__ __forceinline__ void rot_half(uint4& v, const uint4& pv, float4 c0, float4 c1, float4 s0,
+                                         float4 s1) {
+  uint32_t* w = &v.x;
+  const uint32_t* pw = &pv.x;
+  const float cv[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+  const float sv[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+#pragma unroll
+  for (int k = 0; k < 4; ++k)
+    w[k] = rot_pair(w[k], pw[k], cv[2 * k], cv[2 * k + 1], sv[2 * k], sv[2 * k + 1]);
+}
+
+__device__ __forceinline__ uint4 negate_bf16x8(uint4 v) {
+  return make_uint4(v.x ^ 0x80008000u, v.y ^ 0x80008000u, v.z ^ 0x80008000u, v.w ^ 0x80008000u);
+}
+
 // The chunk v (head-local elements j0 .. j0 + 7 of token t's head at src)
 // rotated back; j0 lies in the span.
 template <bool INTERLEAVED>
@@ -78,17 +108,10 @@ __device__ __forceinline__ void rotate_chunk(const RopeParams& p, const uint16_t
     pos = pos < 0 ? 0 : p.P - 1;
   }
   const float* cs = p.cos_sin + (int64_t)pos * p.R;
-  uint32_t* w = &v.x;
-  if (INTERLEAVED) {  // pairs (2k, 2k+1) of the chunk: pair index i0 + k
+  if (INTERLEAVED) {  // pair index i0 + k
     const int i0 = (j0 - p.rope_off) / 2;
-    const float4 cc = __ldg(reinterpret_cast<const float4*>(cs + i0));
-    const float4 ss = __ldg(reinterpret_cast<const float4*>(cs + half + i0));
-    const float cv[4] = {cc.x, cc.y, cc.z, cc.w}, sv[4] = {ss.x, ss.y, ss.z, ss.w};
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {  // (x1, x2) -> (x1 c + x2 s, x2 c + (-x1) s)
-      const uint32_t swapped = __byte_perm(w[k], 0, 0x1032) ^ 0x80000000u;  // (x2, -x1)
-      w[k] = rot_pair(w[k], swapped, cv[k], cv[k], sv[k], sv[k]);
-    }
+    rot_interleaved(v, __ldg(reinterpret_cast<const float4*>(cs + i0)),
+                    __ldg(reinterpret_cast<const float4*>(cs + half + i0)));
     return;
   }
   // rotate-half: the partner chunk lies R/2 elements away in the same head; a
@@ -96,17 +119,29 @@ __device__ __forceinline__ void rotate_chunk(const RopeParams& p, const uint16_t
   const bool first = j0 < p.rope_off + half;
   const int i0 = j0 - p.rope_off - (first ? 0 : half);
   uint4 pv = ldg16(src + (first ? j0 + half : j0 - half));
-  if (!first) pv = make_uint4(pv.x ^ 0x80008000u, pv.y ^ 0x80008000u, pv.z ^ 0x80008000u,
-                              pv.w ^ 0x80008000u);
+  if (!first) pv = negate_bf16x8(pv);
   const float4* c4 = reinterpret_cast<const float4*>(cs + i0);
   const float4* s4 = reinterpret_cast<const float4*>(cs + half + i0);
-  const float4 c0 = __ldg(c4), c1 = __ldg(c4 + 1), s0 = __ldg(s4), s1 = __ldg(s4 + 1);
-  const float cv[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-  const float sv[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
-  const uint32_t* pw = &pv.x;
-#pragma unroll
-  for (int k = 0; k < 4; ++k)
-    w[k] = rot_pair(w[k], pw[k], cv[2 * k], cv[2 * k + 1], sv[2 * k], sv[2 * k + 1]);
+  rot_half(v, pv, __ldg(c4), __ldg(c4 + 1), __ldg(s4), __ldg(s4 + 1));
+}
+
+// The MXFP8 codes of a half block (lane pair = MX block; called by the whole
+// warp) and its E8M0 byte; both lanes of a block store the same byte.
+__device__ __forceinline__ uint4 mx_half_block(const uint4& v0, const uint4& v1, bool ok,
+                                               uint8_t* scale_at) {
+  uint32_t am = absmax8(&v0.x, &v1.x);
+  am = max_nan_bf16x2(am, __shfl_xor_sync(0xFFFFFFFFu, am, 1));
+  const uint32_t code = mx_code(max(am & 0xFFFFu, am >> 16));
+  if (ok) *scale_at = (uint8_t)code;
+  if (code == 0xFFu) return make_uint4(0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
+  const uint32_t sb = (254u - code) << 7;  // bf16 bits of 2^-e (normal: code <= 246)
+  const uint32_t s2 = sb | (sb << 16);
+  const uint32_t* a = &v0.x;
+  const uint32_t* b = &v1.x;
+  return make_uint4(scaled_e4m3_pair(a[0], s2) | (scaled_e4m3_pair(a[1], s2) << 16),
+                    scaled_e4m3_pair(a[2], s2) | (scaled_e4m3_pair(a[3], s2) << 16),
+                    scaled_e4m3_pair(b[0], s2) | (scaled_e4m3_pair(b[1], s2) << 16),
+                    scaled_e4m3_pair(b[2], s2) | (scaled_e4m3_pair(b[3], s2) << 16));
 }
 
 // One loop over units of one kind: a warp takes 64 units at a time, lane l
@@ -166,26 +201,9 @@ __device__ __forceinline__ void unit_loop(const RopeParams& p, const RopeIdx& ix
         }
         continue;
       }
-      const uint32_t* a = &v[j][0].x;
-      const uint32_t* b = &v[j][1].x;
-      uint32_t am = absmax8(a, b);
-      am = max_nan_bf16x2(am, __shfl_xor_sync(0xFFFFFFFFu, am, 1));
-      if (!ok) continue;
-      const uint32_t mag = am;
-      const uint32_t code = mx_code(max(mag & 0xFFFFu, mag >> 16));
-      if ((lane & 1) == 0) p.scale[(int64_t)tk[j] * p.scale_stride + (col >> 5)] = (uint8_t)code;
-      uint4 o;
-      if (code == 0xFFu) {
-        o = make_uint4(0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
-      } else {
-        const uint32_t sb = (254u - code) << 7;  // bf16 bits of 2^-e (normal: code <= 246)
-        const uint32_t s2 = sb | (sb << 16);
-        o = make_uint4(scaled_e4m3_pair(a[0], s2) | (scaled_e4m3_pair(a[1], s2) << 16),
-                       scaled_e4m3_pair(a[2], s2) | (scaled_e4m3_pair(a[3], s2) << 16),
-                       scaled_e4m3_pair(b[0], s2) | (scaled_e4m3_pair(b[1], s2) << 16),
-                       scaled_e4m3_pair(b[2], s2) | (scaled_e4m3_pair(b[3], s2) << 16));
-      }
-      *reinterpret_cast<uint4*>(p.out + (int64_t)tk[j] * p.out_stride + col) = o;
+      const uint4 o = mx_half_block(v[j][0], v[j][1], ok,
+                                    p.scale + (int64_t)tk[j] * p.scale_stride + (col >> 5));
+      if (ok) *reinterpret_cast<uint4*>(p.out + (int64_t)tk[j] * p.out_stride + col) = o;
     }
   }
 }

@@ -236,22 +236,6 @@ __global__ void __launch_bounds__(kWarps * 32, (QS + KS >= 8) ? 2 : 3) rmsnorm_m
   }
 }
 
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
-               : "memory");
-}
-__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
-                                         uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-          dst),
-      "l"(src), "r"(bytes), "r"(bar)
-      : "memory");
-}
-
 // Largest magnitude of four bf16 pairs as bf16 bits, over the four lanes of an
 // MX block (lanes 4b..4b+3); NaN-propagating.
 __device__ __forceinline__ uint32_t absmax2(uint32_t acc, uint32_t y) {  // acc >= 0

@@ -98,6 +98,10 @@ def test_inv_rope_full_workload():
     (7, 3, 96, 16, 64, True), (9, 2, 128, 64, 64, False), (4, 4, 576, 512, 64, False),
     (6, 2, 576, 512, 64, True), (2, 1, 8192, 8064, 128, False), (11, 3, 64, 8, 16, True),
     (13, 2, 64, 0, 0, False), (33, 1, 256, 0, 256, False),
+    # long rows (8 and 9 heads of 8192), the span at the start, the end and absent
+    (3, 8, 8192, 8064, 128, False), (2, 8, 8192, 0, 64, True), (2, 9, 8192, 4096, 0, False),
+    # more tokens than one pass of the grid's warps covers
+    (300, 3, 192, 128, 64, False), (257, 5, 96, 32, 32, True),
 ])
 def test_inv_rope_shapes(T, H, D, off, R, inter):
     rng = np.random.default_rng(T * 7 + D + R)
