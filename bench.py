@@ -602,7 +602,10 @@ def ours(args, rank: int, world: int, local_rank: int) -> None:
 
 def profile_case(args) -> None:
     """One call repeated (for a profiler): the inverse-RoPE producer on the
-    o-projection workload, or the decode-sized gated call."""
+    o-projection workload; the decode-sized gated call; the dynamic per-head
+    quantisation of the first two packed sequences of the static-head workload
+    (its max pass and its quantise pass); or the gated workload with silu as
+    its two unfused steps (gated norm to bf16, then per-token quantisation)."""
     import torch
     import synth
     import rmsnorm_fp8_activation_gb300 as B
@@ -615,6 +618,16 @@ def profile_case(args) -> None:
         o = d16(w.o()).view(w.T, w.H, w.D)
         pos, cs = torch.from_numpy(w.positions()).cuda(), torch.from_numpy(w.cos_sin()).cuda()
         fn = lambda: B.fp8n_inv_rope_quant_mx(o, pos, cs, w.rope_off, w.rope_dim)
+    elif args.case == "dynamic":
+        sw = W["static_head"]
+        ws = synth.StaticHeadWorkload("static_head_2seq", seed=sw.seed, stream_base=sw.stream_base,
+                                      lengths=sw.lengths[:2])
+        Q, K, V = (d16(ws.tensor(k)) for k in ("q", "k", "v"))
+        fn = lambda: B.fp8n_dynamic_head_quant(Q, K, V)
+    elif args.case == "unfused":
+        w = W["gated_silu"]
+        x, g, wt = d16(w.x()), d16(w.gate()), d16(w.weight())
+        fn = lambda: B.fp8n_quant_token(B.fp8n_gated_rmsnorm_bf16(x, g, wt, w.eps, w.act))
     else:
         w = W["gated_small"]
         x, g, wt = d16(w.x()), d16(w.gate()), d16(w.weight())
@@ -633,9 +646,10 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--small", action="store_true",
                     help="profiling case (see make_inputs); prints kernel times only")
-    ap.add_argument("--case", choices=["inv_rope", "decode"], default=None,
-                    help="profiling case: only the inverse-RoPE producer on its workload, or only "
-                         "the decode-sized gated call, --steps times back to back")
+    ap.add_argument("--case", choices=["inv_rope", "decode", "dynamic", "unfused"], default=None,
+                    help="profiling case: only the inverse-RoPE producer on its workload, the "
+                         "decode-sized gated call, the dynamic per-head quantisation, or the "
+                         "unfused gated steps, --steps times back to back")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     world = int(os.environ.get("WORLD_SIZE", "1"))
