@@ -240,21 +240,23 @@ def reference_arm(args, rank: int, world: int) -> None:
     same workload; rank 0 alone under torchrun."""
     if rank != 0:
         return
+    import oracle as O
     inp = make_inputs(0)
+    threads = O.host_threads()
     for _ in range(args.warmup):
-        oracle_sample(inp, *REF_SAMPLE)
+        oracle_sample(inp, *REF_SAMPLE, threads=threads)
     dts, by, desc = [], 0, ""
     for _ in range(args.steps):
-        r = oracle_sample(inp, *REF_SAMPLE)
+        r = oracle_sample(inp, *REF_SAMPLE, threads=threads)
         dts.append(r["seconds"])
-        by, desc = r["bytes"], r["sample"] + ", single-threaded C oracle"
+        by, desc = r["bytes"], r["sample"] + ", the C oracle over row slices on %d host threads" % threads
     total = sum(dts)
     value = by * args.steps / total / 1e9
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64+f32",
             "data": "synthetic", "config": {"workload": WORKLOAD, "sample": desc},
-            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
                              "sample": desc},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
